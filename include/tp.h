@@ -1,0 +1,220 @@
+/*
+ * tp.h -- C ABI of libtp: a warp-specialized, multi-stage, TMA-fed tcgen05
+ * BF16 mainloop for sm_103a (GEMM and its implicit-GEMM convolution form) and
+ * a TMA-only 2D copy.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are caller-owned DEVICE memory (any allocator). The library
+ *    allocates no device memory; its only state is a static device status
+ *    record per GPU and a cached driver entry point.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls are asynchronous on it; they return after the launch.
+ *  - The return value reports what the host can see: invalid arguments, a
+ *    descriptor the driver rejects, a launch error. Device-side failures (a
+ *    bounded barrier wait that gave up) surface through tp_device_status.
+ *  - bf16 is IEEE-style bfloat16; results are rounded to nearest even.
+ *  - Empty problems (a zero M, N, rows or cols) are a no-op returning TP_OK.
+ *    Negative sizes, a leading dimension below the row width, or a NULL
+ *    pointer with a non-empty problem return TP_ERR_INVALID_ARG.
+ *  - A base address or leading dimension that TMA cannot describe (not
+ *    16-byte aligned) is not an error for the copy: it takes the vectorized
+ *    thread-copy path ("B200 Tma Pipeline Designer", step 1 and "Do not use
+ *    when"). For the GEMM and convolution it returns TP_ERR_UNSUPPORTED.
+ */
+#ifndef TP_H
+#define TP_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TP_OK = 0,
+    TP_ERR_INVALID_ARG = 1,
+    TP_ERR_UNSUPPORTED = 2,
+    TP_ERR_CUDA = 3,
+    TP_ERR_DRIVER_ENCODE = 4,
+    TP_ERR_TIMEOUT = 5,
+    TP_ERR_SMEM_BUDGET = 6
+} tp_status;
+
+/* Which code path a call took (tp_plan.path). */
+enum {
+    TP_PATH_NONE = 0,          /* empty problem, nothing launched */
+    TP_PATH_MAINLOOP = 1,      /* TMA + tcgen05 mainloop */
+    TP_PATH_ZERO_FILL = 2,     /* K == 0: C is the empty sum */
+    TP_PATH_TMA_COPY = 3,      /* TMA load -> smem -> TMA store ring */
+    TP_PATH_VEC_COPY = 4       /* vectorized ld/st fallback copy */
+};
+
+/*
+ * C = A . B, bf16 inputs, fp32 accumulation in tensor memory, bf16 output.
+ * Defined by the BF16 GEMM the pipelined mainloop serves ("two-free-pipeline-
+ * stages" note, the 256x128x64 tile) and by the load/compute/store timeline
+ * of "B200 Tma Pipeline Designer", steps 4-7.
+ *   A: M x K row-major, element (i,k) at A[i*lda + k], lda >= K.
+ *   B: K x N column-major, element (k,j) at B[j*ldb + k], ldb >= K.
+ *   C: M x N row-major, element (i,j) at C[i*ldc + j], ldc >= N; overwritten
+ *      (no alpha/beta). K == 0 writes zeros.
+ * TMA needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2 multiples of 16.
+ */
+TP_API int tp_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                 int64_t ldb, int64_t ldc, void* stream);
+
+/* Same as tp_gemm_bf16 with the fp32 accumulator written out (C is float,
+ * ldc*4 a multiple of 16). */
+TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                     int64_t ldb, int64_t ldc, void* stream);
+
+/*
+ * Mainloop choices, for sweeps and tests. Zero fields mean "choose".
+ *   atom:       1 = 1-SM atom (a CTA owns a 128 x tile_n tile and holds all of
+ *               its B tile), 2 = 2-SM atom (a CTA pair owns 256 x tile_n; each
+ *               CTA holds half of B, which frees shared memory for more
+ *               stages: "two-free-pipeline-stages", stage budget table).
+ *   pipe_depth: PIPE_DEPTH, stages in the ring (2..9).
+ *   tile_n:     MMA N (128 or 256).
+ *   group_m:    tile raster: group_m M-tiles share one sweep over N.
+ *   max_ctas:   cap on the persistent grid (0 = one CTA per SM).
+ * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
+ * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
+ * "StageCount<9> fails the capacity assert"; a combination that fits but is
+ * not compiled returns TP_ERR_UNSUPPORTED.
+ */
+typedef struct {
+    int atom;
+    int pipe_depth;
+    int tile_n;
+    int group_m;
+    int max_ctas;
+} tp_gemm_opts;
+
+/* tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit choices (opts may be NULL).
+ * out_f32 selects a float C (1) or a bf16 C (0). */
+TP_API int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                    int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, void* stream);
+
+/*
+ * Forward convolution as an implicit GEMM on the same mainloop; the A tile is
+ * an im2col TMA load ("two-free-pipeline-stages": SM100_TMA_2SM_LOAD_IM2COL).
+ * Cross-correlation, zero padding, no dilation, no groups:
+ *   y[n][p][q][k] = sum_{r,s,c} x[n][p*stride-pad+r][q*stride-pad+s][c] * w[k][r][s][c]
+ *   x: N x H x W x C (NHWC), w: K x R x S x C (KRSC), y: N x P x Q x K
+ *   (NHWC), P = (H + 2 pad - R)/stride + 1, Q = (W + 2 pad - S)/stride + 1.
+ * GEMM view: M = N*P*Q, N = K, K = R*S*C, walked as (r,s) outer, 64-channel
+ * blocks inner. TMA needs C and K multiples of 8, 16-byte aligned buffers,
+ * 1 <= stride <= 8, R, S <= 32 and pad < 128.
+ */
+TP_API int tp_conv2d_fprop_bf16(const void* x_nhwc, const void* w_krsc, void* y_nhwk, int64_t N, int64_t H, int64_t W,
+                         int64_t C, int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad, void* stream);
+
+/* The convolution with explicit mainloop choices and output type. */
+TP_API int tp_conv2d_fprop_bf16_ex(const void* x_nhwc, const void* w_krsc, void* y_nhwk, int64_t N, int64_t H,
+                            int64_t W, int64_t C, int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad,
+                            int out_f32, const tp_gemm_opts* opts, void* stream);
+
+/*
+ * dst = src, bit for bit, for a rows x cols matrix of 2-byte elements, both
+ * buffers with row pitch ld (>= cols) elements. TMA path: a persistent ring
+ * of tiles, TMA load -> shared memory -> TMA store, stores drained with
+ * commit_group / wait_group ("B200 Tma Pipeline Designer", steps 4-7).
+ * Buffers that TMA cannot describe (base not 16-byte aligned, ld*2 not a
+ * multiple of 16) or copies under 64 KiB take the vectorized ld/st path.
+ * src and dst must not overlap; both must be 2-byte aligned.
+ */
+TP_API int tp_tma_copy_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld, void* stream);
+
+/* Copy choices: box_cols x box_rows tiles (box_cols*2 a multiple of 16, both
+ * <= 256), stages in {2,3,4,6,8,12}, ctas_per_sm >= 1, force_vec = 1 takes
+ * the fallback path. Zero fields mean "choose". */
+typedef struct {
+    int box_cols;
+    int box_rows;
+    int stages;
+    int ctas_per_sm;
+    int force_vec;
+} tp_copy_opts;
+
+TP_API int tp_tma_copy_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld,
+                      const tp_copy_opts* opts, void* stream);
+
+/* Synchronizes `stream`, returns the current device's status (TP_OK or the
+ * first device-side failure since the last call, e.g. TP_ERR_TIMEOUT from a
+ * bounded barrier wait) and clears it. Returns TP_ERR_CUDA when the
+ * synchronization itself fails. */
+TP_API int tp_device_status(void* stream);
+
+/* As tp_device_status, also reporting where the failure happened (site code,
+ * block and thread); any output pointer may be NULL. */
+TP_API int tp_device_status_detail(void* stream, int* site, int* block, int* thread);
+
+/* Static string naming a tp_status value. */
+TP_API const char* tp_status_string(int status);
+
+/* The CUDA error code behind the last TP_ERR_CUDA on this thread. */
+TP_API int tp_last_cuda_error(void);
+
+/*
+ * Dynamic shared memory per CTA of the mainloop for (atom, pipe_depth,
+ * tile_n, out_f32): stages x (A 128x64 + B (tile_n/atom)x64 bf16) plus the
+ * epilogue staging, barriers and alignment slack. Writes *bytes and returns
+ * TP_OK when it fits the 232,448-byte opt-in limit, TP_ERR_SMEM_BUDGET when
+ * it does not ("two-free-pipeline-stages", stage budget table), or
+ * TP_ERR_INVALID_ARG for an impossible combination. Host-only; needs no GPU.
+ */
+TP_API int tp_query_smem_bytes(int atom, int pipe_depth, int tile_n, int out_f32, int64_t* bytes);
+
+/* What a call dispatched: the path, the mainloop variant and launch shape. */
+typedef struct {
+    int path;        /* TP_PATH_* */
+    int atom;
+    int pipe_depth;
+    int tile_n;
+    int out_f32;
+    int conv;
+    int grid;        /* CTAs launched */
+    int cluster;     /* CTAs per cluster */
+    int smem_bytes;  /* dynamic shared memory per CTA */
+    int64_t m_tiles, n_tiles, k_blocks;
+} tp_plan;
+
+/*
+ * The plan tp_gemm_bf16_ex would launch for these arguments on a GPU with
+ * sm_count SMs (0 = ask the current device). Host-only when sm_count > 0:
+ * alignment, tile counts, variant choice and shared-memory budget, no launch.
+ * Returns the status tp_gemm_bf16_ex would return before launching.
+ */
+TP_API int tp_gemm_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                 int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* plan);
+
+/* The plan of the last GEMM / conv / copy call made on this thread. */
+TP_API int tp_last_plan(tp_plan* plan);
+
+/* One compiled mainloop variant. */
+typedef struct {
+    int atom, pipe_depth, tile_n, out_f32, conv, smem_bytes;
+} tp_kernel_desc;
+
+/* Writes up to cap compiled variants to out (may be NULL) and returns how
+ * many there are. Host-only. */
+TP_API int tp_list_kernels(tp_kernel_desc* out, int cap);
+
+/* Launches one CTA that waits on an mbarrier nothing arrives on, with a
+ * limit of limit_us microseconds: the wait must give up and record
+ * TP_ERR_TIMEOUT, which tp_device_status then returns. Checks that a stuck
+ * pipeline ends with a status instead of a hang. */
+TP_API int tp_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H */

@@ -1,0 +1,247 @@
+"""Python binding of libtp, the TMA-pipelined tcgen05 BF16 mainloop library.
+
+Argument marshalling only: every entry point passes raw device pointers,
+sizes and a CUDA stream handle to the C ABI declared in include/tp.h, and
+raises TPError on a non-zero status. Tensors (anything with ``data_ptr()``)
+or plain integers are accepted as pointers. PyTorch, when present, only
+supplies device memory and the current stream.
+
+There is no fallback: if libtp.so has not been built, importing the package
+raises. Build it with ``mbarrier_pipelined_tensor_gb300.build.build()`` (or
+``__graft_entry__.build()`` at the repository root).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libtp.so is not built ({LIB_PATH}); run mbarrier_pipelined_tensor_gb300.build.build() first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+TP_OK = 0
+TP_ERR_INVALID_ARG = 1
+TP_ERR_UNSUPPORTED = 2
+TP_ERR_CUDA = 3
+TP_ERR_DRIVER_ENCODE = 4
+TP_ERR_TIMEOUT = 5
+TP_ERR_SMEM_BUDGET = 6
+
+TP_PATH_NONE = 0
+TP_PATH_MAINLOOP = 1
+TP_PATH_ZERO_FILL = 2
+TP_PATH_TMA_COPY = 3
+TP_PATH_VEC_COPY = 4
+
+
+class tp_gemm_opts(ctypes.Structure):
+    _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+
+
+class tp_copy_opts(ctypes.Structure):
+    _fields_ = [("box_cols", ctypes.c_int), ("box_rows", ctypes.c_int), ("stages", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("force_vec", ctypes.c_int)]
+
+
+class tp_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int),
+                ("tile_n", ctypes.c_int), ("out_f32", ctypes.c_int), ("conv", ctypes.c_int),
+                ("grid", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class tp_kernel_desc(ctypes.Structure):
+    _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("out_f32", ctypes.c_int), ("conv", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+
+_SIGS = {
+    "tp_gemm_bf16": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
+    "tp_gemm_bf16_f32": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
+    "tp_gemm_bf16_ex": ([_P, _P, _P] + [_I64] * 6 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
+    "tp_conv2d_fprop_bf16": ([_P, _P, _P] + [_I64] * 9 + [_P], _I),
+    "tp_conv2d_fprop_bf16_ex": ([_P, _P, _P] + [_I64] * 9 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
+    "tp_tma_copy_2d": ([_P, _P, _I64, _I64, _I64, _P], _I),
+    "tp_tma_copy_2d_ex": ([_P, _P, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
+    "tp_device_status": ([_P], _I),
+    "tp_device_status_detail": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "tp_status_string": ([_I], ctypes.c_char_p),
+    "tp_last_cuda_error": ([], _I),
+    "tp_query_smem_bytes": ([_I, _I, _I, _I, ctypes.POINTER(_I64)], _I),
+    "tp_gemm_plan": ([_P, _P, _P] + [_I64] * 6 + [_I, ctypes.POINTER(tp_gemm_opts), _I,
+                                                     ctypes.POINTER(tp_plan)], _I),
+    "tp_last_plan": ([ctypes.POINTER(tp_plan)], _I),
+    "tp_list_kernels": ([ctypes.POINTER(tp_kernel_desc), _I], _I),
+    "tp_selftest_wait_timeout": ([ctypes.c_uint32, _P], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {tp_status_string(status)}"
+        if status == TP_ERR_CUDA:
+            msg += f" (cudaError {_lib.tp_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return 0
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, where: str) -> None:
+    if st != TP_OK:
+        raise TPError(st, where)
+
+
+def tp_status_string(status: int) -> str:
+    return _lib.tp_status_string(status).decode()
+
+
+def tp_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
+    _check(_lib.tp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, _stream(stream)),
+           "tp_gemm_bf16")
+
+
+def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
+    _check(_lib.tp_gemm_bf16_f32(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, _stream(stream)),
+           "tp_gemm_bf16_f32")
+
+
+def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0):
+    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas)
+
+
+def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):
+    o = _opts(**opts)
+    _check(_lib.tp_gemm_bf16_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, int(bool(out_f32)),
+                                ctypes.byref(o), _stream(stream)), "tp_gemm_bf16_ex")
+
+
+def tp_conv2d_fprop_bf16(x, w, y, N, H, W, C, K, R, S, stride, pad, stream=None):
+    _check(_lib.tp_conv2d_fprop_bf16(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad,
+                                     _stream(stream)), "tp_conv2d_fprop_bf16")
+
+
+def tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, out_f32=False, stream=None, **opts):
+    o = _opts(**opts)
+    _check(_lib.tp_conv2d_fprop_bf16_ex(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad,
+                                        int(bool(out_f32)), ctypes.byref(o), _stream(stream)),
+           "tp_conv2d_fprop_bf16_ex")
+
+
+def tp_tma_copy_2d(src, dst, rows, cols, ld, stream=None):
+    _check(_lib.tp_tma_copy_2d(_ptr(src), _ptr(dst), rows, cols, ld, _stream(stream)), "tp_tma_copy_2d")
+
+
+def tp_tma_copy_2d_ex(src, dst, rows, cols, ld, stream=None, box_cols=0, box_rows=0, stages=0,
+                      ctas_per_sm=0, force_vec=False):
+    o = tp_copy_opts(box_cols, box_rows, stages, ctas_per_sm, int(bool(force_vec)))
+    _check(_lib.tp_tma_copy_2d_ex(_ptr(src), _ptr(dst), rows, cols, ld, ctypes.byref(o), _stream(stream)),
+           "tp_tma_copy_2d_ex")
+
+
+def tp_device_status(stream=None) -> int:
+    """Synchronizes the stream; returns (and clears) the device status code."""
+    return int(_lib.tp_device_status(_stream(stream)))
+
+
+def tp_device_status_detail(stream=None):
+    site, block, thread = _I(), _I(), _I()
+    st = _lib.tp_device_status_detail(_stream(stream), ctypes.byref(site), ctypes.byref(block),
+                                      ctypes.byref(thread))
+    return int(st), site.value, block.value, thread.value
+
+
+def tp_query_smem_bytes(atom, pipe_depth, tile_n, out_f32=False):
+    """Returns (status, bytes): TP_OK when it fits, TP_ERR_SMEM_BUDGET when not."""
+    b = _I64()
+    st = _lib.tp_query_smem_bytes(atom, pipe_depth, tile_n, int(bool(out_f32)), ctypes.byref(b))
+    return int(st), int(b.value)
+
+
+def tp_gemm_plan(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, sm_count=0, **opts):
+    """Returns (status, plan dict) without launching anything."""
+    o = _opts(**opts)
+    p = tp_plan()
+    st = _lib.tp_gemm_plan(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, int(bool(out_f32)),
+                           ctypes.byref(o), sm_count, ctypes.byref(p))
+    return int(st), p.as_dict()
+
+
+def tp_last_plan() -> dict:
+    p = tp_plan()
+    _check(_lib.tp_last_plan(ctypes.byref(p)), "tp_last_plan")
+    return p.as_dict()
+
+
+def tp_list_kernels():
+    n = _lib.tp_list_kernels(None, 0)
+    arr = (tp_kernel_desc * n)()
+    _lib.tp_list_kernels(arr, n)
+    return [{f: getattr(a, f) for f, _ in tp_kernel_desc._fields_} for a in arr]
+
+
+def tp_selftest_wait_timeout(limit_us: int, stream=None):
+    _check(_lib.tp_selftest_wait_timeout(limit_us, _stream(stream)), "tp_selftest_wait_timeout")
+
+
+# --------------------------------------------------------------------------
+# Tensor conveniences (still marshalling only: shapes -> sizes and pitches).
+# --------------------------------------------------------------------------
+
+def gemm(A, B_nk, C, stream=None, **opts):
+    """C (M x N, bf16 or fp32) = A (M x K) . B, B given as an N x K tensor
+    (i.e. K x N column-major). Row pitches come from the tensors' strides."""
+    M, K = A.shape
+    N = B_nk.shape[0]
+    out_f32 = str(C.dtype).endswith("float32")
+    tp_gemm_bf16_ex(A, B_nk, C, M, N, K, A.stride(0), B_nk.stride(0), C.stride(0), out_f32=out_f32,
+                    stream=stream, **opts)
+    return C
+
+
+def conv2d_fprop(x, w, y, stride=1, pad=0, stream=None, **opts):
+    """y (N x P x Q x K) = conv(x (N x H x W x C), w (K x R x S x C))."""
+    N, H, W, C = x.shape
+    K, R, S, _ = w.shape
+    out_f32 = str(y.dtype).endswith("float32")
+    tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, out_f32=out_f32, stream=stream, **opts)
+    return y

@@ -1,0 +1,576 @@
+// C ABI of libtp (declared in include/tp.h): argument checks, TMA-vs-fallback
+// dispatch ("B200 Tma Pipeline Designer", step 1), tensor-map construction
+// (step 2; "CUDA 13 TMA Descriptor Notes": byte strides, BFLOAT16 type),
+// mainloop variant choice against the shared-memory budget
+// ("two-free-pipeline-stages", stage budget table) and the device status
+// record.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm_kernel.cuh"
+#include "tensor_map.h"
+#include "tp.h"
+
+namespace tp {
+const KernelEntry* table_mainloop_cg1(int* n);
+const KernelEntry* table_mainloop_cg2(int* n);
+const KernelEntry* table_mainloop_conv(int* n);
+cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensorMap& d, const CopyParams& p,
+                                int grid, cudaStream_t st);
+int copy_smem_bytes(int stages, uint32_t tile_bytes);
+cudaError_t launch_vec_copy(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld, int sm_count,
+                            cudaStream_t st);
+cudaError_t launch_zero_fill(void* c, int64_t M, int64_t N, int64_t ldc, int elem_bytes, cudaStream_t st);
+cudaError_t launch_wait_selftest(const WaitCtl& w, cudaStream_t st);
+}  // namespace tp
+
+using namespace tp;
+
+namespace {
+
+__device__ DevStatus g_status;  // one per device that loads the library
+
+constexpr int kMaxSmemPerCta = 232448;  // sm_100-class opt-in limit (227 KiB)
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready;
+    int sm_count;
+    DevStatus* status;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+thread_local int t_last_cuda_error = 0;
+thread_local tp_plan t_last_plan = {};
+
+int cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return TP_ERR_CUDA;
+}
+
+int device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return TP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d.sm_count = sms;
+        d.status = static_cast<DevStatus*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return TP_OK;
+}
+
+uint64_t wait_limit_ns()
+{
+    static uint64_t v = [] {
+        const char* s = std::getenv("TP_WAIT_LIMIT_MS");
+        long ms = s ? std::strtol(s, nullptr, 10) : 0;
+        if (ms <= 0) ms = 4000;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------ variant table ---
+
+struct Tables {
+    const KernelEntry* t[3];
+    int n[3];
+};
+
+const Tables& tables()
+{
+    static Tables tb = [] {
+        Tables x{};
+        x.t[0] = table_mainloop_cg1(&x.n[0]);
+        x.t[1] = table_mainloop_cg2(&x.n[1]);
+        x.t[2] = table_mainloop_conv(&x.n[2]);
+        return x;
+    }();
+    return tb;
+}
+
+const KernelEntry* find_kernel(const KernelKey& k)
+{
+    const Tables& tb = tables();
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < tb.n[i]; ++j) {
+            const KernelKey& e = tb.t[i][j].key;
+            if (e.cta_group == k.cta_group && e.bn == k.bn && e.stages == k.stages && e.out_f32 == k.out_f32 &&
+                e.conv == k.conv)
+                return &tb.t[i][j];
+        }
+    return nullptr;
+}
+
+// Mirrors MainloopCfg::SMEM_BYTES.
+int64_t mainloop_smem(int atom, int depth, int tile_n)
+{
+    const int64_t a = 128 * 64 * 2;
+    const int64_t b = static_cast<int64_t>(tile_n / atom) * 64 * 2;
+    const int64_t epi = 4 * 2 * 32 * 128;
+    return 1024 + depth * (a + b) + epi + 256;
+}
+
+int deepest_fitting(int atom, int tile_n)
+{
+    int d = 9;
+    while (d > 2 && mainloop_smem(atom, d, tile_n) > kMaxSmemPerCta) --d;
+    return d;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Variant and launch shape for a GEMM view M x N x K (k_blocks given).
+int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv, const tp_gemm_opts* o,
+                  int sm_count, tp_plan* pl)
+{
+    int atom = o && o->atom ? o->atom : 0;
+    int tile_n = o && o->tile_n ? o->tile_n : 0;
+    if (atom != 0 && atom != 1 && atom != 2) return TP_ERR_INVALID_ARG;
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256) return TP_ERR_INVALID_ARG;
+    if (atom == 0) atom = 1;
+    if (tile_n == 0) tile_n = 128;
+    int depth = o && o->pipe_depth ? o->pipe_depth : deepest_fitting(atom, tile_n);
+    if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
+    const int64_t smem = mainloop_smem(atom, depth, tile_n);
+    if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
+    const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv});
+    if (!k) return TP_ERR_UNSUPPORTED;
+
+    const int64_t m_tiles = cdiv(M, 128 * atom);
+    const int64_t n_tiles = cdiv(N, tile_n);
+    const int64_t tiles = m_tiles * n_tiles;
+    if (tiles > (1ll << 31) - 1 || k_blocks > (1ll << 31) - 1) return TP_ERR_UNSUPPORTED;
+    int64_t clusters = sm_count / atom;
+    if (o && o->max_ctas > 0) clusters = std::max<int64_t>(1, o->max_ctas / atom);
+    if (clusters > tiles) clusters = tiles;
+    if (clusters < 1) clusters = 1;
+
+    pl->path = TP_PATH_MAINLOOP;
+    pl->atom = atom;
+    pl->pipe_depth = depth;
+    pl->tile_n = tile_n;
+    pl->out_f32 = out_f32;
+    pl->conv = conv;
+    pl->grid = static_cast<int>(clusters * atom);
+    pl->cluster = atom;
+    pl->smem_bytes = k->smem_bytes;
+    pl->m_tiles = m_tiles;
+    pl->n_tiles = n_tiles;
+    pl->k_blocks = k_blocks;
+    return TP_OK;
+}
+
+int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
+{
+    int g = o && o->group_m > 0 ? o->group_m : 16;
+    if (g > m_tiles) g = static_cast<int>(m_tiles);
+    return g < 1 ? 1 : g;
+}
+
+int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                   int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* pl)
+{
+    std::memset(pl, 0, sizeof(*pl));
+    if (M < 0 || N < 0 || K < 0) return TP_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TP_OK;
+    if (lda < K || ldb < K || ldc < N) return TP_ERR_INVALID_ARG;
+    if (!C || (K > 0 && (!A || !B))) return TP_ERR_INVALID_ARG;
+    const int eb = out_f32 ? 4 : 2;
+    if (K == 0) {
+        pl->path = TP_PATH_ZERO_FILL;
+        pl->out_f32 = out_f32;
+        return TP_OK;
+    }
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TP_ERR_UNSUPPORTED;
+    // TMA suitability: 16-byte aligned bases and byte pitches.
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda * 2) % 16 || (ldb * 2) % 16 || (ldc * eb) % 16)
+        return TP_ERR_UNSUPPORTED;
+    return plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, opts, sm_count, pl);
+}
+
+int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
+{
+    const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv});
+    if (!k) return TP_ERR_UNSUPPORTED;
+    L.grid = pl.grid;
+    L.stream = st;
+    cudaError_t e = k->launch(L);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return TP_OK;
+}
+
+}  // namespace
+
+// ===================================================================== ABI ==
+
+extern "C" {
+
+const char* tp_status_string(int s)
+{
+    switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA";
+    case TP_ERR_DRIVER_ENCODE: return "TP_ERR_DRIVER_ENCODE";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    case TP_ERR_SMEM_BUDGET: return "TP_ERR_SMEM_BUDGET";
+    default: return "TP_ERR_UNKNOWN";
+    }
+}
+
+int tp_last_cuda_error(void) { return t_last_cuda_error; }
+
+int tp_last_plan(tp_plan* plan)
+{
+    if (!plan) return TP_ERR_INVALID_ARG;
+    *plan = t_last_plan;
+    return TP_OK;
+}
+
+int tp_query_smem_bytes(int atom, int pipe_depth, int tile_n, int out_f32, int64_t* bytes)
+{
+    (void)out_f32;  // the staging buffers are 128-byte rows for either output type
+    if ((atom != 1 && atom != 2) || (tile_n != 128 && tile_n != 256) || pipe_depth < 1 || !bytes)
+        return TP_ERR_INVALID_ARG;
+    *bytes = mainloop_smem(atom, pipe_depth, tile_n);
+    return *bytes <= kMaxSmemPerCta ? TP_OK : TP_ERR_SMEM_BUDGET;
+}
+
+int tp_list_kernels(tp_kernel_desc* out, int cap)
+{
+    const Tables& tb = tables();
+    int n = 0;
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < tb.n[i]; ++j, ++n) {
+            if (out && n < cap) {
+                const KernelEntry& e = tb.t[i][j];
+                out[n] = tp_kernel_desc{e.key.cta_group, e.key.stages, e.key.bn, e.key.out_f32, e.key.conv,
+                                        e.smem_bytes};
+            }
+        }
+    return n;
+}
+
+int tp_gemm_plan(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                 int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* plan)
+{
+    if (!plan) return TP_ERR_INVALID_ARG;
+    if (sm_count <= 0) {
+        DeviceState* d = nullptr;
+        int st = device_state(&d);
+        if (st) return st;
+        sm_count = d->sm_count;
+    }
+    return gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32 ? 1 : 0, opts, sm_count, plan);
+}
+
+int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                    int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, void* stream)
+{
+    out_f32 = out_f32 ? 1 : 0;
+    tp_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    t_last_plan = pl;
+    if (M < 0 || N < 0 || K < 0) return TP_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TP_OK;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, dev->sm_count, &pl);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.path == TP_PATH_ZERO_FILL) {
+        cudaError_t e = launch_zero_fill(C, M, N, ldc, out_f32 ? 4 : 2, s);
+        t_last_plan = pl;
+        return e == cudaSuccess ? TP_OK : cuda_fail(e);
+    }
+    const int cg = pl.atom;
+    const int b_rows = pl.tile_n / cg;
+    GemmLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
+                 {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
+                 {64, 128}, CU_TENSOR_MAP_SWIZZLE_128B};
+    TiledDesc db{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B),
+                 {static_cast<uint64_t>(K), static_cast<uint64_t>(N)}, {static_cast<uint64_t>(ldb) * 2},
+                 {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
+    const uint32_t eb = out_f32 ? 4 : 2;
+    const int64_t n_tma = N / (16 / eb) * (16 / eb);
+    TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
+                 {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
+                 {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+    if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db)) || (st = encode_tiled(&L.mapC, dc)))
+        return st;
+    GemmParams& p = L.params;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.m_tiles = static_cast<int>(pl.m_tiles);
+    p.n_tiles = static_cast<int>(pl.n_tiles);
+    p.k_blocks = static_cast<int>(pl.k_blocks);
+    p.group_m = group_m_for(opts, pl.m_tiles);
+    p.n_tma = static_cast<int>(n_tma);
+    p.C = C;
+    p.ldc_bytes = ldc * eb;
+    p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    st = launch_plan(pl, L, s);
+    if (st == TP_OK) t_last_plan = pl;
+    return st;
+}
+
+int tp_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                 int64_t ldb, int64_t ldc, void* stream)
+{
+    return tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, 0, nullptr, stream);
+}
+
+int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                     int64_t ldb, int64_t ldc, void* stream)
+{
+    return tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, 1, nullptr, stream);
+}
+
+int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, int64_t H, int64_t W, int64_t C,
+                            int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad, int out_f32,
+                            const tp_gemm_opts* opts, void* stream)
+{
+    out_f32 = out_f32 ? 1 : 0;
+    tp_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    t_last_plan = pl;
+    if (N < 0 || H < 0 || W < 0 || C < 0 || K < 0 || R < 1 || S < 1 || stride < 1 || pad < 0)
+        return TP_ERR_INVALID_ARG;
+    const int64_t hp = H + 2 * pad - R, wp = W + 2 * pad - S;
+    if (hp < 0 || wp < 0) return TP_ERR_INVALID_ARG;
+    const int64_t P = hp / stride + 1, Q = wp / stride + 1;
+    const int64_t M = N * P * Q;
+    if (M == 0 || K == 0) return TP_OK;
+    if (!y || (C > 0 && (!x || !w))) return TP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (C == 0) {
+        pl.path = TP_PATH_ZERO_FILL;
+        cudaError_t e = launch_zero_fill(y, M, K, K, out_f32 ? 4 : 2, s);
+        t_last_plan = pl;
+        return e == cudaSuccess ? TP_OK : cuda_fail(e);
+    }
+    // im2col TMA limits (cuTensorMapEncodeIm2col: rank-4 corners in
+    // [-128, 127], traversal strides <= 8) and 16-byte byte strides.
+    if (C % 8 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(y) || stride > 8 || R > 32 || S > 32 ||
+        pad > 127 || M > INT32_MAX || N * H * W > INT32_MAX)
+        return TP_ERR_UNSUPPORTED;
+    const int64_t cblocks = cdiv(C, 64);
+    st = plan_mainloop(M, K, R * S * cblocks, out_f32, 1, opts, dev->sm_count, &pl);
+    if (st) return st;
+    const int cg = pl.atom;
+    const int b_rows = pl.tile_n / cg;
+    GemmLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    Im2colDesc dx{};
+    dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    dx.base = const_cast<void*>(x);
+    dx.dims[0] = static_cast<uint64_t>(C);
+    dx.dims[1] = static_cast<uint64_t>(W);
+    dx.dims[2] = static_cast<uint64_t>(H);
+    dx.dims[3] = static_cast<uint64_t>(N);
+    dx.strides_bytes[0] = static_cast<uint64_t>(C) * 2;
+    dx.strides_bytes[1] = static_cast<uint64_t>(W * C) * 2;
+    dx.strides_bytes[2] = static_cast<uint64_t>(H * W * C) * 2;
+    // Bounding box of the filter window's first tap: from -pad to
+    // (extent - 1) + pad - (filter - 1), the positions output pixels start at.
+    dx.lower[0] = static_cast<int>(-pad);
+    dx.lower[1] = static_cast<int>(-pad);
+    dx.upper[0] = static_cast<int>(pad - (S - 1));
+    dx.upper[1] = static_cast<int>(pad - (R - 1));
+    dx.channels = 64;
+    dx.pixels = 128;
+    dx.elem_strides[0] = 1;
+    dx.elem_strides[1] = static_cast<uint32_t>(stride);
+    dx.elem_strides[2] = static_cast<uint32_t>(stride);
+    dx.elem_strides[3] = 1;
+    dx.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (dx.upper[0] < -128 || dx.upper[1] < -128) return TP_ERR_UNSUPPORTED;
+    TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w),
+                 {static_cast<uint64_t>(C), static_cast<uint64_t>(R * S), static_cast<uint64_t>(K)},
+                 {static_cast<uint64_t>(C) * 2, static_cast<uint64_t>(R * S * C) * 2},
+                 {64, 1, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
+    const uint32_t eb = out_f32 ? 4 : 2;
+    TiledDesc dy{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y,
+                 {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
+                 {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+    if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw)) || (st = encode_tiled(&L.mapC, dy)))
+        return st;
+    GemmParams& p = L.params;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(K);
+    p.K = static_cast<int>(R * S * C);
+    p.m_tiles = static_cast<int>(pl.m_tiles);
+    p.n_tiles = static_cast<int>(pl.n_tiles);
+    p.k_blocks = static_cast<int>(pl.k_blocks);
+    p.group_m = group_m_for(opts, pl.m_tiles);
+    p.conv_P = static_cast<int>(P);
+    p.conv_Q = static_cast<int>(Q);
+    p.conv_stride = static_cast<int>(stride);
+    p.conv_pad = static_cast<int>(pad);
+    p.conv_S = static_cast<int>(S);
+    p.conv_cblocks = static_cast<int>(cblocks);
+    p.n_tma = static_cast<int>(K);  // K % 8 == 0: rows are whole 16-byte granules
+    p.C = y;
+    p.ldc_bytes = K * eb;
+    p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    st = launch_plan(pl, L, s);
+    if (st == TP_OK) t_last_plan = pl;
+    return st;
+}
+
+int tp_conv2d_fprop_bf16(const void* x, const void* w, void* y, int64_t N, int64_t H, int64_t W, int64_t C,
+                         int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad, void* stream)
+{
+    return tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, 0, nullptr, stream);
+}
+
+int tp_tma_copy_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld,
+                      const tp_copy_opts* o, void* stream)
+{
+    tp_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    t_last_plan = pl;
+    if (rows < 0 || cols < 0 || ld < cols) return TP_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return TP_OK;
+    if (!src || !dst) return TP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 1u) return TP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int box_cols = o && o->box_cols ? o->box_cols : 64;
+    const int box_rows = o && o->box_rows ? o->box_rows : 128;
+    const int stages = o && o->stages ? o->stages : 8;
+    const int per_sm = o && o->ctas_per_sm ? o->ctas_per_sm : 1;
+    if (box_cols < 8 || box_cols > 256 || (box_cols * 2) % 16 || box_rows < 1 || box_rows > 256 || per_sm < 1)
+        return TP_ERR_INVALID_ARG;
+    const bool tma_ok = aligned16(src) && aligned16(dst) && (ld * 2) % 16 == 0 && rows * cols * 2 >= 65536 &&
+                        rows <= INT32_MAX && cols <= INT32_MAX && !(o && o->force_vec);
+    if (!tma_ok) {
+        cudaError_t e = launch_vec_copy(src, dst, rows, cols, ld, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        pl.path = TP_PATH_VEC_COPY;
+        t_last_plan = pl;
+        return TP_OK;
+    }
+    // TMA stores write whole 16-byte granules of a row: the TMA ring copies
+    // the first cols_tma columns, the ragged tail goes through the
+    // vectorized path.
+    const int64_t cols_tma = cols / 8 * 8;
+    if (cols_tma == 0) {
+        cudaError_t e = launch_vec_copy(src, dst, rows, cols, ld, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        pl.path = TP_PATH_VEC_COPY;
+        t_last_plan = pl;
+        return TP_OK;
+    }
+    const uint32_t tile_bytes = static_cast<uint32_t>(box_cols * box_rows * 2);
+    const int smem = copy_smem_bytes(stages, tile_bytes);
+    if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
+    TiledDesc d{CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(src),
+                {static_cast<uint64_t>(cols_tma), static_cast<uint64_t>(rows)}, {static_cast<uint64_t>(ld) * 2},
+                {static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows)}, CU_TENSOR_MAP_SWIZZLE_NONE};
+    CUtensorMap ms, md;
+    if ((st = encode_tiled(&ms, d))) return st;
+    d.base = dst;
+    if ((st = encode_tiled(&md, d))) return st;
+    CopyParams p{};
+    p.tiles_x = static_cast<int>(cdiv(cols_tma, box_cols));
+    p.tiles_y = static_cast<int>(cdiv(rows, box_rows));
+    p.box_cols = box_cols;
+    p.box_rows = box_rows;
+    p.tile_bytes = tile_bytes;
+    p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    const int64_t tiles = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
+    if (tiles > INT32_MAX) return TP_ERR_UNSUPPORTED;
+    int64_t grid = static_cast<int64_t>(dev->sm_count) * per_sm;
+    if (grid > tiles) grid = tiles;
+    cudaError_t e = launch_tma_copy_any(stages, ms, md, p, static_cast<int>(grid), s);
+    if (e == cudaErrorInvalidValue && stages != 2 && stages != 3 && stages != 4 && stages != 6 && stages != 8 &&
+        stages != 12)
+        return TP_ERR_INVALID_ARG;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cols_tma < cols) {
+        e = launch_vec_copy(static_cast<const uint16_t*>(src) + cols_tma, static_cast<uint16_t*>(dst) + cols_tma,
+                            rows, cols - cols_tma, ld, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    pl.path = TP_PATH_TMA_COPY;
+    pl.pipe_depth = stages;
+    pl.grid = static_cast<int>(grid);
+    pl.cluster = 1;
+    pl.smem_bytes = smem;
+    pl.m_tiles = p.tiles_y;
+    pl.n_tiles = p.tiles_x;
+    t_last_plan = pl;
+    return TP_OK;
+}
+
+int tp_tma_copy_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld, void* stream)
+{
+    return tp_tma_copy_2d_ex(src, dst, rows, cols, ld, nullptr, stream);
+}
+
+int tp_device_status_detail(void* stream, int* site, int* block, int* thread)
+{
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    DevStatus h{};
+    e = cudaMemcpy(&h, dev->status, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (h.code != 0) {
+        DevStatus z{};
+        e = cudaMemcpy(dev->status, &z, sizeof(z), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (site) *site = h.site;
+    if (block) *block = h.block;
+    if (thread) *thread = h.thread;
+    return h.code;
+}
+
+int tp_device_status(void* stream) { return tp_device_status_detail(stream, nullptr, nullptr, nullptr); }
+
+int tp_selftest_wait_timeout(uint32_t limit_us, void* stream)
+{
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    if (limit_us == 0 || limit_us > 10u * 1000u * 1000u) return TP_ERR_INVALID_ARG;
+    WaitCtl w{dev->status, static_cast<uint64_t>(limit_us) * 1000ull};
+    cudaError_t e = launch_wait_selftest(w, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
+}  // extern "C"

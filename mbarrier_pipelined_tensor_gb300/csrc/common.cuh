@@ -1,0 +1,135 @@
+// Definitions shared by the kernels and the host launchers: the device status
+// record, bounded barrier waits and the kernel parameter blocks.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace tp {
+
+// Status codes (same values as tp_status in include/tp.h).
+enum : int {
+    ST_OK = 0,
+    ST_INVALID_ARG = 1,
+    ST_UNSUPPORTED = 2,
+    ST_CUDA = 3,
+    ST_DRIVER_ENCODE = 4,
+    ST_TIMEOUT = 5,
+    ST_SMEM_BUDGET = 6,
+};
+
+// Where a bounded wait gave up (recorded with ST_TIMEOUT).
+enum : int {
+    SITE_PRODUCER_EMPTY = 1,
+    SITE_MMA_FULL = 2,
+    SITE_MMA_ACC_EMPTY = 3,
+    SITE_EPI_ACC_FULL = 4,
+    SITE_COPY_FULL = 5,
+    SITE_DRAIN = 6,
+    SITE_SELFTEST = 7,
+};
+
+// One per device, a static __device__ object of the library. The first
+// failure wins; tp_device_status reads and clears it.
+struct DevStatus {
+    int code;
+    int site;
+    int block;
+    int thread;
+};
+
+struct WaitCtl {
+    DevStatus* status;
+    uint64_t limit_ns;  // give up after this long without progress
+};
+
+__device__ __forceinline__ void report_failure(DevStatus* st, int code, int site)
+{
+    if (atomicCAS(&st->code, 0, code) == 0) {
+        st->site = site;
+        st->block = static_cast<int>(blockIdx.x);
+        st->thread = static_cast<int>(threadIdx.x);
+    }
+}
+
+// Wait for the phase of parity `parity` of `bar` to complete. Gives up after
+// w.limit_ns (or ~2^30 polls), records ST_TIMEOUT at `site`, raises the
+// CTA's abort flag and returns false; also returns false as soon as another
+// role of the CTA raised the flag. Never traps.
+template <bool CLUSTER_SCOPE>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                             volatile int* abort_flag, int site)
+{
+    auto poll = [&]() {
+        return CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (poll()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (poll()) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.limit_ns || i > (1u << 30)) {
+                report_failure(w.status, ST_TIMEOUT, site);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// GEMM view of a launch. For the convolution M = N*P*Q output pixels,
+// N = output channels, K = R*S*C (walked as (r, s) outer, 64-channel blocks
+// inner).
+struct GemmParams {
+    int M, N, K;
+    // TMA stores write whole 16-byte granules of a row, so the C map ends at
+    // the last full granule (n_tma columns); columns n_tma..N-1 are written
+    // with plain stores through C / ldc_bytes.
+    int n_tma;
+    void* C;
+    int64_t ldc_bytes;
+    int m_tiles;   // tiles of 128*CG rows
+    int n_tiles;   // tiles of BN columns
+    int k_blocks;  // 64-deep K blocks
+    int group_m;   // tile raster: group_m M-tiles share a sweep over N
+    // convolution only
+    int conv_P, conv_Q, conv_stride, conv_pad, conv_S, conv_cblocks;
+    WaitCtl wait;
+};
+
+struct CopyParams {
+    int tiles_x, tiles_y;      // tiles along columns / rows
+    int box_cols, box_rows;
+    uint32_t tile_bytes;
+    WaitCtl wait;
+};
+
+// Key of one compiled GEMM/conv mainloop.
+struct KernelKey {
+    int cta_group;  // 1 or 2
+    int bn;         // MMA N (pair tile N for cta_group 2)
+    int stages;     // PIPE_DEPTH
+    int out_f32;
+    int conv;
+};
+
+struct GemmLaunch {
+    CUtensorMap mapA, mapB, mapC;
+    GemmParams params;
+    int grid;
+    cudaStream_t stream;
+};
+
+using GemmLauncher = cudaError_t (*)(const GemmLaunch&);
+
+struct KernelEntry {
+    KernelKey key;
+    GemmLauncher launch;
+    int smem_bytes;
+};
+
+}  // namespace tp

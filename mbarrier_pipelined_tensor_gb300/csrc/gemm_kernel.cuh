@@ -1,0 +1,420 @@
+// Warp-specialized, persistent, TMA-fed tcgen05 BF16 mainloop: C = A.B with
+// fp32 accumulation in TMEM, and its implicit-GEMM (im2col) convolution form.
+//
+// Roles (192 threads, 6 warps):
+//   warp 0      producer: the lane picked by elect.sync waits for a free
+//               stage, posts arrive.expect_tx on the stage's full barrier and
+//               issues the TMA loads -- the same thread does both, so the one
+//               arrival a stage expects always comes from the issuing lane
+//               (CUTLASS issue #3722, "Expected behavior").
+//   warp 1      MMA issuer and TMEM owner: waits full[s], issues 4 tcgen05.mma
+//               (K = 16 each) per 64-deep stage, commits to empty[s]; after a
+//               tile's last stage commits to acc_full[b].
+//   warps 2..5  epilogue: wait acc_full[b], read TMEM with tcgen05.ld, free
+//               the accumulator (acc_empty[b]) as soon as it is read, convert,
+//               stage through swizzled shared memory and write C with TMA
+//               stores drained by commit_group / wait_group.
+//
+// Stage ring ("B200 Tma Pipeline Designer", steps 4-7): PIPE_DEPTH stages of
+// A (128x64 bf16) and B; full[s] / empty[s] each have exactly one producer
+// and one consumer; initial phases let the producer's first pass through the
+// ring run without waiting. Two TMEM accumulators let the epilogue of tile
+// t-1 overlap the mainloop of tile t (the "store k-1" of the steady state).
+//
+// Atoms ("two-free-pipeline-stages" note): CG = 1 is the 1-SM atom (each CTA
+// owns a 128 x BN tile and holds all of its B tile); CG = 2 is the 2-SM atom
+// (a CTA pair owns 256 x BN, the leader issues cta_group::2 MMAs, and each
+// CTA holds only its half of B, which is what frees shared memory for more
+// stages at the same budget).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace tp {
+
+template <int CG, int BN, int STAGES, bool OUT_F32>
+struct MainloopCfg {
+    static constexpr int BM = 128;  // rows per CTA (TMEM lanes)
+    static constexpr int BK = 64;   // one 128-byte swizzle row of bf16
+    static constexpr int UMMA_K = 16;
+    static constexpr int B_ROWS = BN / CG;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;  // the leader's expect_tx covers the pair
+    static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
+    static constexpr int EPI_COLS = 128 / OUT_BYTES;  // columns per 128-byte staging row
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_BUF = 32 * 128;  // one warp's 32 rows x 128 B
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_BUF;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static constexpr int THREADS = 192;
+
+    static_assert(BN % (16 * CG) == 0 && BN >= 32 && BN <= 256, "UMMA N");
+    static_assert(B_BYTES % 1024 == 0, "B stage must hold whole swizzle atoms");
+    static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
+                  "TMEM allocation must be a power of two");
+    static_assert(BN % EPI_COLS == 0, "epilogue chunking");
+    static_assert(2 * STAGES + 5 <= (BAR_BYTES - 8) / 8, "barrier area");
+};
+
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt)
+{
+    const int group = p.group_m * p.n_tiles;
+    const int g = t / group;
+    const int first = g * p.group_m;
+    const int gm = min(p.m_tiles - first, p.group_m);
+    const int r = t - g * group;
+    mt = first + r % gm;
+    nt = r / gm;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+__global__ void __launch_bounds__(192, 1)
+    mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapC, const GemmParams p)
+{
+    using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
+    constexpr bool CL = (CG == 2);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzle atoms need 1024-B alignment
+    uint8_t* const base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base;
+    const uint32_t sB = sA + STAGES * Cfg::A_BYTES;
+    const uint32_t sEpi = sB + STAGES * Cfg::B_BYTES;
+    const uint32_t sBar = sEpi + Cfg::EPI_BYTES;
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+    auto empty_bar = [&](int s) { return sBar + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return sBar + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return sBar + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = sBar + 8u * (2 * STAGES + 4);
+    uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + (sBar - base) + 8 * (2 * STAGES + 5));
+    volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rank = CL ? cluster_ctarank() : 0u;
+    const bool leader = (rank == 0);
+
+    // ------------------------------------------------------------ setup ---
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);   // one arrival: the producer's expect_tx
+            mbar_init(empty_bar(s), 1);  // one arrival: the MMA issuer's commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), Cfg::EPI_WARPS * CG);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&mapA);
+        prefetch_tensormap(&mapB);
+        prefetch_tensormap(&mapC);
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tcgen05_fence_before();
+    if constexpr (CL) cluster_sync(); else __syncthreads();
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+    if (warp == 0) {
+        // --------------------------------------------------- producer ---
+        if (elect_one()) {
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+                int mt, nt;
+                tile_coords(t, p, mt, nt);
+                const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
+                const int n_row = nt * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+                int img = 0, base_h = 0, base_w = 0;
+                if constexpr (CONV) {
+                    const int pq = p.conv_P * p.conv_Q;
+                    img = m_row / pq;
+                    const int rem = m_row - img * pq;
+                    const int pp = rem / p.conv_Q;
+                    const int qq = rem - pp * p.conv_Q;
+                    base_h = pp * p.conv_stride - p.conv_pad;
+                    base_w = qq * p.conv_stride - p.conv_pad;
+                }
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded<CL>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = CL ? mapa_shared(full_bar(s), 0) : full_bar(s);
+                    if (leader) mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
+                    const uint32_t dA = sA + s * Cfg::A_BYTES;
+                    const uint32_t dB = sB + s * Cfg::B_BYTES;
+                    if constexpr (CONV) {
+                        const int rs = kb / p.conv_cblocks;
+                        const int c0 = (kb - rs * p.conv_cblocks) * Cfg::BK;
+                        const int r = rs / p.conv_S;
+                        const int sx = rs - r * p.conv_S;
+                        if constexpr (CL) {
+                            tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img,
+                                                    static_cast<uint16_t>(sx), static_cast<uint16_t>(r));
+                            tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row);
+                        } else {
+                            tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img,
+                                               static_cast<uint16_t>(sx), static_cast<uint16_t>(r));
+                            tma_load_3d(dB, &mapB, fb, c0, rs, n_row);
+                        }
+                    } else {
+                        if constexpr (CL) {
+                            tma_load_2d_pair(dA, &mapA, fb, kb * Cfg::BK, m_row);
+                            tma_load_2d_pair(dB, &mapB, fb, kb * Cfg::BK, n_row);
+                        } else {
+                            tma_load_2d(dA, &mapA, fb, kb * Cfg::BK, m_row);
+                            tma_load_2d(dB, &mapB, fb, kb * Cfg::BK, n_row);
+                        }
+                    }
+                    ++issued;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok && (!CL || leader)) {
+                // Gave up: let the loads already in flight land before the
+                // CTA's shared memory can be released (bounded as well).
+                WaitCtl drain = p.wait;
+                int n = issued < STAGES ? issued : STAGES;
+                int ss = s;
+                uint32_t pp = ph;
+                volatile int no_abort = 0;
+                for (int i = 0; i < n; ++i) {
+                    if (--ss < 0) {
+                        ss = STAGES - 1;
+                        pp ^= 1u;
+                    }
+                    wait_bounded<CL>(full_bar(ss), pp, drain, &no_abort, SITE_DRAIN);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ---
+        if (!CL || leader) {
+            if (elect_one()) {
+                constexpr uint32_t IDESC = umma_idesc_bf16_f32(Cfg::BM * CG, BN);
+                int s = 0;
+                uint32_t ph = 0;
+                int lt = 0;
+                bool ok = true;
+                for (int t = cluster_id; ok && t < num_tiles; t += num_clusters, ++lt) {
+                    const int b = lt & 1;
+                    const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+                    if (!wait_bounded<CL>(acce_bar(b), aph ^ 1u, p.wait, abort_flag, SITE_MMA_ACC_EMPTY)) break;
+                    tcgen05_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                    for (int kb = 0; kb < p.k_blocks; ++kb) {
+                        if (!wait_bounded<CL>(full_bar(s), ph, p.wait, abort_flag, SITE_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tcgen05_fence_after();
+                        const uint32_t aS = sA + s * Cfg::A_BYTES;
+                        const uint32_t bS = sB + s * Cfg::B_BYTES;
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
+                            const uint64_t da = umma_desc_sw128_kmajor(aS + k * 32);
+                            const uint64_t db = umma_desc_sw128_kmajor(bS + k * 32);
+                            umma_bf16<CG>(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
+                        else umma_commit(empty_bar(s));
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if constexpr (CL) umma_commit_pair(accf_bar(b), 0x3);
+                    else umma_commit(accf_bar(b));
+                }
+                // Every MMA this thread issued completes before teardown.
+                if constexpr (CL) umma_commit_pair(drain_bar, 0x1);
+                else umma_commit(drain_bar);
+                volatile int no_abort = 0;
+                wait_bounded<CL>(drain_bar, 0, p.wait, &no_abort, SITE_DRAIN);
+            }
+            __syncwarp();
+        }
+    } else {
+        // --------------------------------------------------- epilogue ---
+        const int ew = warp - 2;           // staging slot of this warp
+        const int quarter = warp & 3;      // TMEM lanes this warp may read
+        const uint32_t stage0 = sEpi + static_cast<uint32_t>(ew) * 2u * Cfg::EPI_BUF;
+        constexpr int CHUNKS = BN / Cfg::EPI_COLS;
+        int buf = 0;
+        int lt = 0;
+        for (int t = cluster_id; t < num_tiles; t += num_clusters, ++lt) {
+            const int b = lt & 1;
+            const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+            if (!wait_bounded<CL>(accf_bar(b), aph, p.wait, abort_flag, SITE_EPI_ACC_FULL)) break;
+            tcgen05_fence_after();
+            int mt, nt;
+            tile_coords(t, p, mt, nt);
+            const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM + quarter * 32;
+            const int n0 = nt * BN;
+            int nchunks = 0;
+            if (m_row < p.M) {
+                nchunks = (p.N - n0 + Cfg::EPI_COLS - 1) / Cfg::EPI_COLS;
+                nchunks = nchunks < CHUNKS ? nchunks : CHUNKS;
+            }
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(b * BN);
+            const uint32_t acce_target = CL ? mapa_shared(acce_bar(b), 0) : acce_bar(b);
+            if (nchunks == 0) {
+                tcgen05_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CL) mbar_arrive_cluster(acce_target);
+                    else mbar_arrive(acce_target);
+                }
+                continue;
+            }
+            for (int c = 0; c < nchunks; ++c) {
+                uint32_t packed[32];
+                if constexpr (OUT_F32) {
+                    tmem_ld_32x32b_x32(t_row + c * 32, packed);
+                    tmem_wait_ld();
+                } else {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(t_row + c * 64, v0);
+                    tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        packed[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                        packed[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+                    }
+                }
+                if (c == nchunks - 1) {
+                    // Accumulator fully read: hand it back to the MMA issuer.
+                    tcgen05_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CL) mbar_arrive_cluster(acce_target);
+                        else mbar_arrive(acce_target);
+                    }
+                }
+                const int cs = n0 + c * Cfg::EPI_COLS;
+                if (cs < p.n_tma) {
+                    // The staging buffer about to be written was last used two
+                    // chunks ago; its TMA store must have finished reading it.
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    const uint32_t sbuf = stage0 + static_cast<uint32_t>(buf) * Cfg::EPI_BUF;
+                    const uint32_t row_addr = sbuf + lane * 128u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t slot = static_cast<uint32_t>(j) ^ (lane & 7u);
+                        st_shared_v4(row_addr + slot * 16u, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                     packed[4 * j + 3]);
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&mapC, sbuf, cs, m_row);
+                        bulk_commit_group();
+                    }
+                    buf ^= 1;
+                }
+                if (cs + Cfg::EPI_COLS > p.n_tma) {
+                    // Columns past the last full 16-byte granule of the row.
+                    const int lo = (p.n_tma > cs ? p.n_tma : cs) - cs;
+                    const int hi = (p.N - cs < Cfg::EPI_COLS ? p.N - cs : Cfg::EPI_COLS);
+                    const int row = m_row + static_cast<int>(lane);
+                    if (row < p.M && lo < hi) {
+                        uint8_t* rowp = static_cast<uint8_t*>(p.C) + static_cast<int64_t>(row) * p.ldc_bytes;
+#pragma unroll
+                        for (int j = 0; j < Cfg::EPI_COLS; ++j) {
+                            if (j >= lo && j < hi) {
+                                if constexpr (OUT_F32)
+                                    reinterpret_cast<uint32_t*>(rowp)[cs + j] = packed[j];
+                                else
+                                    reinterpret_cast<uint16_t*>(rowp)[cs + j] =
+                                        static_cast<uint16_t>(packed[j >> 1] >> (16 * (j & 1)));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // --------------------------------------------------------- teardown ---
+    tcgen05_fence_before();
+    if constexpr (CL) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tcgen05_fence_after();
+        tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+cudaError_t launch_mainloop(const GemmLaunch& L)
+{
+    using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
+    auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.params);
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+constexpr KernelEntry mainloop_entry()
+{
+    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0},
+                       &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV>,
+                       MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES};
+}
+
+}  // namespace tp

@@ -1,0 +1,100 @@
+#include "tensor_map.h"
+
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace tp {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_tiled = nullptr;
+PFN_cuTensorMapEncodeIm2col_v12000 g_im2col = nullptr;
+std::once_flag g_once;
+bool g_found = false;
+
+void resolve()
+{
+    std::call_once(g_once, [] {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+        cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1) ==
+                cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000, cudaEnableDefault, &q2) ==
+                cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            g_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+            g_im2col = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(f2);
+            g_found = true;
+        }
+    });
+}
+
+uint32_t elem_bytes(CUtensorMapDataType t)
+{
+    switch (t) {
+    case CU_TENSOR_MAP_DATA_TYPE_UINT8: return 1;
+    case CU_TENSOR_MAP_DATA_TYPE_UINT16:
+    case CU_TENSOR_MAP_DATA_TYPE_FLOAT16:
+    case CU_TENSOR_MAP_DATA_TYPE_BFLOAT16: return 2;
+    case CU_TENSOR_MAP_DATA_TYPE_FLOAT64:
+    case CU_TENSOR_MAP_DATA_TYPE_UINT64:
+    case CU_TENSOR_MAP_DATA_TYPE_INT64: return 8;
+    default: return 4;
+    }
+}
+
+}  // namespace
+
+bool tiled_ok(const TiledDesc& d)
+{
+    if (d.rank < 1 || d.rank > 5) return false;
+    if ((reinterpret_cast<uintptr_t>(d.base) & 15u) != 0) return false;
+    const uint32_t eb = elem_bytes(d.dtype);
+    for (uint32_t i = 0; i < d.rank; ++i) {
+        if (d.dims[i] == 0 || d.dims[i] > (1ull << 32)) return false;
+        if (d.box[i] == 0 || d.box[i] > 256) return false;
+    }
+    for (uint32_t i = 0; i + 1 < d.rank; ++i) {
+        if (d.strides_bytes[i] % 16 != 0 || d.strides_bytes[i] >= (1ull << 40)) return false;
+    }
+    if ((d.box[0] * eb) % 16 != 0) return false;
+    if (d.swizzle == CU_TENSOR_MAP_SWIZZLE_128B && d.box[0] * eb > 128) return false;
+    return true;
+}
+
+int encode_tiled(CUtensorMap* out, const TiledDesc& d)
+{
+    resolve();
+    if (!g_found) return ST_CUDA;
+    if (!tiled_ok(d)) return ST_INVALID_ARG;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_tiled(out, d.dtype, d.rank, d.base, reinterpret_cast<const cuuint64_t*>(d.dims),
+                         reinterpret_cast<const cuuint64_t*>(d.strides_bytes),
+                         reinterpret_cast<const cuuint32_t*>(d.box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         d.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ST_OK : ST_DRIVER_ENCODE;
+}
+
+int encode_im2col(CUtensorMap* out, const Im2colDesc& d)
+{
+    resolve();
+    if (!g_found) return ST_CUDA;
+    if ((reinterpret_cast<uintptr_t>(d.base) & 15u) != 0) return ST_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (d.strides_bytes[i] % 16 != 0) return ST_INVALID_ARG;
+    CUresult r = g_im2col(out, d.dtype, 4, d.base, reinterpret_cast<const cuuint64_t*>(d.dims),
+                          reinterpret_cast<const cuuint64_t*>(d.strides_bytes), d.lower, d.upper, d.channels,
+                          d.pixels, reinterpret_cast<const cuuint32_t*>(d.elem_strides),
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, d.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ST_OK : ST_DRIVER_ENCODE;
+}
+
+}  // namespace tp

@@ -1,0 +1,75 @@
+"""GPU parity of the 2-SM atom (a cluster of two CTAs issuing cta_group::2
+MMAs, each CTA holding half of the B tile: "two-free-pipeline-stages", "The
+atom changes the fragment") against the CPU oracle, for every compiled ring
+depth, both MMA N, ragged pair tiles and the convolution."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import datagen  # noqa: E402
+import oracle  # noqa: E402
+import mbarrier_pipelined_tensor_gb300 as tp  # noqa: E402
+from gpu_util import check_against_oracle, dev_bf16, expect_ok, host_f64, new_out, run_gemm  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+ONE = np.uint16(0x3F80)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_atom2_ragged_config(tile_n, out_f32):
+    M, N, K = 320, 200, 448       # pair tile 256 rows: the second pair's upper CTA is all out of bounds
+    A, B = datagen.gemm_operands(M, N, K, seed=0)
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=out_f32, atom=2, tile_n=tile_n)
+    assert plan["atom"] == 2 and plan["cluster"] == 2 and plan["grid"] % 2 == 0
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, out_f32, f"atom2 n{tile_n}")
+
+
+def test_atom2_identity_bit_exact():
+    M = K = 512
+    N = 384
+    A = np.where(np.eye(M, K, dtype=bool), ONE, np.uint16(0)).astype(np.uint16)
+    B = datagen.Stream(13).uniform_bf16((N, K))
+    for tile_n in (128, 256):
+        got, _ = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=2, tile_n=tile_n)
+        assert np.array_equal(got, datagen.bf16_to_f32(B).astype(np.float64).T)
+
+
+ATOM2 = [(128, d) for d in range(2, 9)] + [(256, d) for d in range(2, 7)]
+
+
+@pytest.mark.parametrize("tile_n,depth", ATOM2)
+def test_atom2_every_depth(tile_n, depth):
+    M, N, K = 600, 520, 1216
+    A, B = datagen.gemm_operands(M, N, K, seed=32)
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=False, atom=2, tile_n=tile_n, pipe_depth=depth)
+    assert (plan["atom"], plan["tile_n"], plan["pipe_depth"]) == (2, tile_n, depth)
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, False, f"atom2 n{tile_n} d{depth}")
+
+
+def test_atom2_persistent_small_grid():
+    M, N, K = 1280, 1024, 384
+    A, B = datagen.gemm_operands(M, N, K, seed=42)
+    for tile_n in (128, 256):
+        got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=2, tile_n=tile_n, max_ctas=4, group_m=2)
+        assert plan["grid"] == 4
+        ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+        check_against_oracle(got, ref, ab, True, f"atom2 persistent n{tile_n}")
+
+
+@pytest.mark.parametrize("tile_n,out_f32", [(128, False), (128, True), (256, False)])
+def test_atom2_conv(tile_n, out_f32):
+    N, H, W, C, K, R, S, st, pad = 2, 13, 11, 96, 256, 3, 3, 1, 1
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=22)
+    P, Q = oracle.conv_out_hw(H, W, R, S, st, pad)
+    y = new_out(N * P * Q, K, out_f32)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, st, pad, out_f32=out_f32,
+                               atom=2, tile_n=tile_n)
+    expect_ok()
+    assert tp.tp_last_plan()["atom"] == 2
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, st, pad)
+    check_against_oracle(host_f64(y), ref, ab, out_f32, "atom2 conv")

@@ -1,0 +1,249 @@
+"""GPU parity of the TMA copy, the 1-SM mainloop and the implicit-GEMM conv
+against the CPU oracle, on seeded inputs small enough to check every element
+yet spanning several tiles, ragged tails and varied K_TILES ("B200 Tma
+Pipeline Designer", step 8: asymmetric small matrices, boundary tiles,
+different K_TILES). Every call goes through the C ABI.
+
+Tolerance (fp32 accumulator): |gpu - ref| <= 1e-3 * sum|a*b| + 1e-6 per
+element; bf16 outputs add half a bf16 ulp, 2**-8 * |ref|. Copies, and GEMMs
+whose every partial sum is exact in fp32 (identity, permutation, all-ones),
+must match bit for bit.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import datagen  # noqa: E402
+import oracle  # noqa: E402
+import mbarrier_pipelined_tensor_gb300 as tp  # noqa: E402
+from gpu_util import (check_against_oracle, dev_bf16, dev_u16, expect_ok, host_f64, host_u16,  # noqa: E402
+                      new_out, run_gemm)
+
+pytestmark = pytest.mark.gpu
+
+ONE = np.uint16(0x3F80)
+
+
+# ------------------------------------------------------------------ copy ---
+
+@pytest.mark.parametrize("rows,cols,ld", [(300, 1000, 1000), (257, 130, 136), (1024, 64, 64), (128, 4096, 4104),
+                                           (515, 1003, 1016)])
+def test_tma_copy_bit_exact_ragged(rows, cols, ld):
+    src_h = datagen.copy_source(rows, cols, seed=4, ld=ld)
+    src = dev_u16(src_h)
+    dst = torch.full_like(src, 0x5A5A)
+    tp.tp_tma_copy_2d(src, dst, rows, cols, ld)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_TMA_COPY
+    got = host_u16(dst)
+    assert np.array_equal(got[:, :cols], src_h[:, :cols])
+    assert np.all(got[:, cols:] == 0x5A5A), "copy wrote into the pitch padding"
+
+
+@pytest.mark.parametrize("box_cols,box_rows,stages,per_sm", [(64, 128, 2, 1), (64, 128, 12, 1), (256, 32, 6, 2),
+                                                             (128, 64, 4, 3), (8, 256, 3, 1)])
+def test_tma_copy_ring_shapes(box_cols, box_rows, stages, per_sm):
+    rows, cols, ld = 777, 1500, 1504
+    src_h = datagen.copy_source(rows, cols, seed=5, ld=ld)
+    src = dev_u16(src_h)
+    dst = torch.zeros_like(src)
+    tp.tp_tma_copy_2d_ex(src, dst, rows, cols, ld, box_cols=box_cols, box_rows=box_rows, stages=stages,
+                         ctas_per_sm=per_sm)
+    expect_ok()
+    p = tp.tp_last_plan()
+    assert p["path"] == tp.TP_PATH_TMA_COPY and p["pipe_depth"] == stages
+    assert np.array_equal(host_u16(dst), src_h)
+
+
+@pytest.mark.parametrize("rows,cols,ld,offset", [(100, 1001, 1001, 0), (64, 600, 600, 1), (3, 5, 7, 0),
+                                                 (200, 512, 520, 3)])
+def test_vectorized_fallback_copy(rows, cols, ld, offset):
+    total = rows * ld + 16
+    src_h = datagen.Stream(6).bits16((total,))
+    src_all = dev_u16(src_h)
+    dst_all = torch.full_like(src_all, 0x1234)
+    src = src_all[offset:]
+    dst = dst_all[offset:]
+    tp.tp_tma_copy_2d(src, dst, rows, cols, ld)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_COPY
+    got = host_u16(dst_all)
+    want = np.full_like(src_h, 0x1234)
+    for r in range(rows):
+        s = offset + r * ld
+        want[s:s + cols] = src_h[s:s + cols]
+    assert np.array_equal(got, want)
+
+
+def test_forced_fallback_matches_tma():
+    rows, cols = 512, 2048
+    src_h = datagen.copy_source(rows, cols, seed=7)
+    src = dev_u16(src_h)
+    d1, d2 = torch.zeros_like(src), torch.zeros_like(src)
+    tp.tp_tma_copy_2d(src, d1, rows, cols, cols)
+    tp.tp_tma_copy_2d_ex(src, d2, rows, cols, cols, force_vec=True)
+    expect_ok()
+    assert torch.equal(d1, src) and torch.equal(d2, src)
+
+
+def test_copy_empty_and_invalid():
+    src = torch.zeros(16, dtype=torch.int16, device="cuda")
+    tp.tp_tma_copy_2d(src, src, 0, 5, 5)
+    with pytest.raises(tp.TPError):
+        tp.tp_tma_copy_2d(src, src, 2, 5, 4)
+
+
+# ------------------------------------------------------------ bounded wait ---
+
+def test_bounded_wait_gives_up_with_status():
+    tp.tp_selftest_wait_timeout(2000)
+    st, site, block, thread = tp.tp_device_status_detail()
+    assert st == tp.TP_ERR_TIMEOUT and site == 7
+    assert tp.tp_device_status() == tp.TP_OK  # cleared
+    # The context is still usable.
+    src = dev_u16(datagen.copy_source(256, 256, seed=8))
+    dst = torch.zeros_like(src)
+    tp.tp_tma_copy_2d(src, dst, 256, 256, 256)
+    expect_ok()
+    assert torch.equal(src, dst)
+
+
+# ---------------------------------------------------------- GEMM, 1-SM ---
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_gemm_ragged_config_every_element(out_f32):
+    M, N, K = 320, 200, 448
+    A, B = datagen.gemm_operands(M, N, K, seed=0)
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=out_f32)
+    assert plan["path"] == tp.TP_PATH_MAINLOOP and plan["k_blocks"] == 7
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, out_f32, "320x200x448")
+
+
+def test_gemm_left_identity_bit_exact():
+    M = K = 192
+    N = 320
+    A = np.where(np.eye(M, K, dtype=bool), ONE, np.uint16(0)).astype(np.uint16)
+    B = datagen.Stream(11).uniform_bf16((N, K))
+    got, _ = run_gemm(A, B, M, N, K, K, K, out_f32=True)
+    assert np.array_equal(got, datagen.bf16_to_f32(B).astype(np.float64).T)
+
+
+def test_gemm_permutation_bit_exact():
+    M = K = 256
+    N = 136
+    perm = np.random.default_rng(3).permutation(K)
+    A = np.zeros((M, K), dtype=np.uint16)
+    A[np.arange(M), perm] = ONE
+    B = datagen.Stream(12).uniform_bf16((N, K))
+    got, _ = run_gemm(A, B, M, N, K, K, K, out_f32=True)
+    assert np.array_equal(got, datagen.bf16_to_f32(B).astype(np.float64)[:, perm].T)
+    got16, _ = run_gemm(A, B, M, N, K, K, K, out_f32=False)
+    assert np.array_equal(got16, datagen.bf16_to_f32(B).astype(np.float64)[:, perm].T)
+
+
+@pytest.mark.parametrize("K", [64, 1000, 4096])
+def test_gemm_all_ones_is_k(K):
+    M, N = 136, 264
+    A = np.full((M, K), ONE, dtype=np.uint16)
+    B = np.full((N, K), ONE, dtype=np.uint16)
+    got, _ = run_gemm(A, B, M, N, K, K, K, out_f32=True)
+    assert np.all(got == K)
+
+
+@pytest.mark.parametrize("M", [1, 127, 129, 200])
+@pytest.mark.parametrize("N", [1, 64, 129, 200])
+@pytest.mark.parametrize("K", [16, 40, 448, 1001])
+def test_gemm_shape_grid(M, N, K):
+    lda = ldb = (K + 7) // 8 * 8
+    A, B = datagen.gemm_operands(M, N, K, seed=M * 7 + N * 13 + K, lda=lda, ldb=ldb)
+    ldc = (N + 7) // 8 * 8
+    got, plan = run_gemm(A, B, M, N, K, lda, ldb, ldc=ldc, out_f32=(M + N) % 2 == 0)
+    assert plan["k_blocks"] == (K + 63) // 64
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    check_against_oracle(got, ref, ab, (M + N) % 2 == 0, f"{M}x{N}x{K}")
+
+
+def test_gemm_pitched_operands_with_poisoned_padding():
+    M, N, K = 300, 260, 520
+    lda, ldb, ldc = K + 24, K + 40, N + 20
+    A, B = datagen.gemm_operands(M, N, K, seed=21, lda=lda, ldb=ldb)
+    for out_f32 in (True, False):
+        got, _ = run_gemm(A, B, M, N, K, lda, ldb, ldc=ldc, out_f32=out_f32)
+        ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+        check_against_oracle(got, ref, ab, out_f32, "pitched")
+
+
+def test_gemm_k_zero_writes_zeros():
+    M, N = 37, 70
+    a = torch.zeros(8, dtype=torch.bfloat16, device="cuda")
+    c = new_out(M, 72, True)
+    tp.tp_gemm_bf16_ex(a, a, c, M, N, 0, 8, 8, 72, out_f32=True)
+    expect_ok()
+    h = c.cpu().numpy()
+    assert np.all(h[:, :N] == 0) and np.all(np.isnan(h[:, N:]))
+
+
+ATOM1 = [(128, d) for d in range(2, 7)] + [(256, d) for d in range(2, 5)]
+
+
+@pytest.mark.parametrize("tile_n,depth", ATOM1)
+def test_gemm_atom1_every_depth(tile_n, depth):
+    M, N, K = 520, 600, 1216  # 19 K-blocks: more than, and not a multiple of, every depth
+    A, B = datagen.gemm_operands(M, N, K, seed=31)
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=False, atom=1, tile_n=tile_n, pipe_depth=depth)
+    assert (plan["atom"], plan["tile_n"], plan["pipe_depth"]) == (1, tile_n, depth)
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, False, f"atom1 n{tile_n} d{depth}")
+
+
+def test_gemm_persistent_many_tiles_small_grid():
+    # Few CTAs, many tiles: each CTA loops through tiles, the two TMEM
+    # accumulators alternate and the stage ring wraps many times.
+    M, N, K = 1024, 1024, 320
+    A, B = datagen.gemm_operands(M, N, K, seed=41)
+    for tile_n in (128, 256):
+        got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, tile_n=tile_n, max_ctas=3, group_m=3)
+        assert plan["grid"] == 3
+        ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+        check_against_oracle(got, ref, ab, True, f"persistent n{tile_n}")
+
+
+# ------------------------------------------------------------------ conv ---
+
+CONV_CASES = [
+    # N, H, W, C, K, R, S, stride, pad
+    (2, 9, 7, 64, 64, 3, 3, 1, 1),
+    (1, 12, 10, 16, 72, 3, 3, 1, 1),      # C < 64: channel overhang zero-filled
+    (2, 11, 9, 128, 200, 3, 3, 2, 1),     # stride 2, ragged N
+    (3, 6, 6, 96, 128, 1, 1, 1, 0),       # 1x1
+    (1, 10, 13, 32, 64, 3, 5, 1, 2),      # R != S, pad 2
+    (2, 7, 7, 8, 8, 3, 3, 1, 0),          # no padding, tiny C
+]
+
+
+@pytest.mark.parametrize("case", CONV_CASES)
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_conv_small_every_element(case, out_f32):
+    N, H, W, C, K, R, S, st, pad = case
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=2)
+    P, Q = oracle.conv_out_hw(H, W, R, S, st, pad)
+    y = new_out(N * P * Q, K, out_f32)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, st, pad, out_f32=out_f32,
+                               atom=1)
+    expect_ok()
+    assert tp.tp_last_plan()["conv"] == 1
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, st, pad)
+    check_against_oracle(host_f64(y), ref, ab, out_f32, f"conv {case}")
+
+
+def test_conv_centre_delta_bit_exact():
+    N, H, W, C = 2, 16, 12, 64
+    x = datagen.Stream(9).uniform_bf16((N, H, W, C))
+    w = np.zeros((C, 3, 3, C), dtype=np.uint16)
+    w[np.arange(C), 1, 1, np.arange(C)] = ONE
+    y = new_out(N * H * W, C, True)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, C, 3, 3, 1, 1, out_f32=True, atom=1)
+    expect_ok()
+    assert np.array_equal(host_f64(y), datagen.bf16_to_f32(x).astype(np.float64).reshape(-1, C))

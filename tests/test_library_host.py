@@ -1,0 +1,159 @@
+"""Host-side checks of libtp that need no GPU: the library loads and exports
+every entry point include/tp.h declares, the shared-memory budget reproduces
+the stage table of the "two-free-pipeline-stages" note, and the dispatch plan
+(TMA suitability, tile counts, variant choice) is right."""
+import os
+import re
+
+import pytest
+
+import mbarrier_pipelined_tensor_gb300 as tp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tp.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "stage_budget.txt")
+SM_COUNT = 152
+SMEM_LIMIT = 232448
+AL = 1 << 20  # a 16-byte aligned fake device address (nothing is launched)
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^TP_API\s+(?:const\s+char\s*\*|int)\s+(tp_\w+)\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(tp._lib, n), n
+    assert sorted(names) == sorted(tp.EXPORTED)
+
+
+def test_status_strings():
+    assert tp.tp_status_string(tp.TP_OK) == "TP_OK"
+    assert tp.tp_status_string(tp.TP_ERR_SMEM_BUDGET) == "TP_ERR_SMEM_BUDGET"
+    assert tp.tp_status_string(99) == "TP_ERR_UNKNOWN"
+
+
+# ------------------------------------------------------ stage budget -----
+
+def golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.split("#")[0].strip()
+        if line:
+            atom, stages, val = line.split()
+            rows.append((int(atom), int(stages), None if val == "FAIL" else int(val)))
+    return rows
+
+
+def page_stage_bytes(atom):
+    # Tile 256x128x64 on a 2x1x1 cluster: a CTA's A fragment is 128x64 bf16;
+    # the 1-SM atom holds the whole 128-row N-side tile, the 2-SM atom half.
+    return 128 * 64 * 2 + (128 // atom) * 64 * 2
+
+
+def test_golden_budget_table_is_consistent_arithmetic():
+    rows = golden_rows()
+    (a0, s0, b0) = rows[0]
+    other = b0 - s0 * page_stage_bytes(a0)          # the other smem tenants
+    assert other == 34816
+    for atom, stages, val in rows:
+        total = stages * page_stage_bytes(atom) + other
+        if val is None:
+            assert total > SMEM_LIMIT, (atom, stages, total)
+        else:
+            assert total == val and total <= SMEM_LIMIT
+
+
+def test_library_budget_reproduces_page_depths():
+    # Our kernel's other tenants differ from the page's, but the deepest ring
+    # per atom, the failing depths and the identical budget at the deepest
+    # ring come out the same.
+    rows = golden_rows()
+    fits = {}
+    for atom in (1, 2):
+        fits[atom] = [d for d in range(2, 12) if tp.tp_query_smem_bytes(atom, d, 128)[0] == tp.TP_OK]
+    deepest = {a: max(fits[a]) for a in fits}
+    for atom, stages, val in rows:
+        if val is None:
+            st, b = tp.tp_query_smem_bytes(atom, stages, 128)
+            assert st == tp.TP_ERR_SMEM_BUDGET and b > SMEM_LIMIT
+        else:
+            assert deepest[atom] == stages
+    b1 = tp.tp_query_smem_bytes(1, deepest[1], 128)[1]
+    b2 = tp.tp_query_smem_bytes(2, deepest[2], 128)[1]
+    assert b1 == b2 <= SMEM_LIMIT
+
+
+def test_query_rejects_impossible():
+    assert tp.tp_query_smem_bytes(3, 4, 128)[0] == tp.TP_ERR_INVALID_ARG
+    assert tp.tp_query_smem_bytes(1, 4, 96)[0] == tp.TP_ERR_INVALID_ARG
+
+
+def test_compiled_variants_match_budget():
+    ks = tp.tp_list_kernels()
+    assert len(ks) >= 20
+    for k in ks:
+        st, b = tp.tp_query_smem_bytes(k["atom"], k["pipe_depth"], k["tile_n"], k["out_f32"])
+        assert st == tp.TP_OK and b == k["smem_bytes"], k
+    sweep = {(k["atom"], k["pipe_depth"]) for k in ks if k["tile_n"] == 128 and not k["conv"] and not k["out_f32"]}
+    assert {(1, d) for d in range(2, 7)} <= sweep
+    assert {(2, d) for d in range(2, 9)} <= sweep
+
+
+# ------------------------------------------------------------- plans -----
+
+def plan(M, N, K, lda=None, ldb=None, ldc=None, A=AL, B=AL, C=AL, out_f32=False, **opts):
+    lda = K if lda is None else lda
+    ldb = K if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return tp.tp_gemm_plan(A, B, C, M, N, K, lda, ldb, ldc, out_f32=out_f32, sm_count=SM_COUNT, **opts)
+
+
+def test_plan_ragged_small_config():
+    st, p = plan(320, 200, 448)
+    assert st == tp.TP_OK and p["path"] == tp.TP_PATH_MAINLOOP
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (3, 2, 7)
+    assert p["grid"] == 6 and p["smem_bytes"] <= SMEM_LIMIT
+
+
+def test_plan_big_square_grid_is_persistent():
+    st, p = plan(8192, 8192, 8192)
+    assert st == tp.TP_OK and p["grid"] == SM_COUNT
+    st, p = plan(8192, 8192, 8192, atom=2, tile_n=256)
+    assert st == tp.TP_OK and p["cluster"] == 2 and p["grid"] == SM_COUNT
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 32, 128)
+
+
+def test_plan_k_tiles_ragged():
+    for K, kt in [(16, 1), (40, 1), (64, 1), (65, 2), (1000, 16), (1001, 16), (16384, 256)]:
+        st, p = plan(128, 128, K, lda=(K + 7) // 8 * 8, ldb=(K + 7) // 8 * 8)
+        assert st == tp.TP_OK and p["k_blocks"] == kt, K
+
+
+def test_plan_edge_cases():
+    assert plan(0, 5, 7)[0] == tp.TP_OK and plan(0, 5, 7)[1]["path"] == tp.TP_PATH_NONE
+    st, p = plan(5, 7, 0, lda=8, ldb=8, ldc=8)
+    assert st == tp.TP_OK and p["path"] == tp.TP_PATH_ZERO_FILL
+    assert plan(-1, 5, 7)[0] == tp.TP_ERR_INVALID_ARG
+    assert plan(4, 4, 16, lda=8)[0] == tp.TP_ERR_INVALID_ARG          # lda < K
+    assert plan(4, 4, 16, ldc=2)[0] == tp.TP_ERR_INVALID_ARG          # ldc < N
+    assert plan(4, 4, 16, A=0)[0] == tp.TP_ERR_INVALID_ARG            # NULL A
+
+
+def test_plan_tma_suitability():
+    assert plan(64, 64, 64, A=AL + 2)[0] == tp.TP_ERR_UNSUPPORTED     # base not 16-B aligned
+    assert plan(64, 64, 60, lda=60)[0] == tp.TP_ERR_UNSUPPORTED       # lda*2 = 120 not a multiple of 16
+    assert plan(64, 60, 64, ldc=60, out_f32=True)[0] == tp.TP_OK      # 60*4 = 240 = 15*16
+    assert plan(64, 60, 64, ldc=60)[0] == tp.TP_ERR_UNSUPPORTED       # 60*2 = 120
+
+
+def test_plan_budget_errors():
+    assert plan(256, 256, 256, atom=2, pipe_depth=9)[0] == tp.TP_ERR_SMEM_BUDGET
+    assert plan(256, 256, 256, atom=1, pipe_depth=7)[0] == tp.TP_ERR_SMEM_BUDGET
+    assert plan(256, 256, 256, atom=1, tile_n=256, pipe_depth=5)[0] == tp.TP_ERR_SMEM_BUDGET
+    assert plan(256, 256, 256, atom=3)[0] == tp.TP_ERR_INVALID_ARG
+    st, p = plan(256, 256, 256, atom=2, pipe_depth=8)
+    assert st == tp.TP_OK and p["pipe_depth"] == 8
