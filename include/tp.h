@@ -17,9 +17,11 @@
  *    Negative sizes, a leading dimension below the row width, or a NULL
  *    pointer with a non-empty problem return TP_ERR_INVALID_ARG.
  *  - A base address or leading dimension that TMA cannot describe (not
- *    16-byte aligned) is not an error for the copy: it takes the vectorized
- *    thread-copy path ("B200 Tma Pipeline Designer", step 1 and "Do not use
- *    when"). For the GEMM and convolution it returns TP_ERR_UNSUPPORTED.
+ *    16-byte aligned) is not an error: the copy takes the vectorized thread
+ *    copy, the GEMM and convolution a plain-load producer that feeds the same
+ *    tcgen05 mainloop ("B200 Tma Pipeline Designer", step 1 and "Do not use
+ *    when"). Elements must still be naturally aligned (2 bytes for bf16, 4
+ *    for a float C), else TP_ERR_INVALID_ARG.
  */
 #ifndef TP_H
 #define TP_H
@@ -52,7 +54,8 @@ enum {
     TP_PATH_MAINLOOP = 1,      /* TMA + tcgen05 mainloop */
     TP_PATH_ZERO_FILL = 2,     /* K == 0: C is the empty sum */
     TP_PATH_TMA_COPY = 3,      /* TMA load -> smem -> TMA store ring */
-    TP_PATH_VEC_COPY = 4       /* vectorized ld/st fallback copy */
+    TP_PATH_VEC_COPY = 4,      /* vectorized ld/st fallback copy */
+    TP_PATH_FALLBACK_MAINLOOP = 5  /* plain-load producer + tcgen05 mainloop */
 };
 
 /*
@@ -64,7 +67,9 @@ enum {
  *   B: K x N column-major, element (k,j) at B[j*ldb + k], ldb >= K.
  *   C: M x N row-major, element (i,j) at C[i*ldc + j], ldc >= N; overwritten
  *      (no alpha/beta). K == 0 writes zeros.
- * TMA needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2 multiples of 16.
+ * The TMA producer needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2
+ * multiples of 16; other layouts take the plain-load producer (1-SM atom,
+ * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED).
  */
 TP_API int tp_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                  int64_t ldb, int64_t ldc, void* stream);
@@ -110,8 +115,9 @@ TP_API int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int
  *   x: N x H x W x C (NHWC), w: K x R x S x C (KRSC), y: N x P x Q x K
  *   (NHWC), P = (H + 2 pad - R)/stride + 1, Q = (W + 2 pad - S)/stride + 1.
  * GEMM view: M = N*P*Q, N = K, K = R*S*C, walked as (r,s) outer, 64-channel
- * blocks inner. TMA needs C and K multiples of 8, 16-byte aligned buffers,
- * 1 <= stride <= 8, R, S <= 32 and pad < 128.
+ * blocks inner. The im2col TMA producer needs C and K multiples of 8,
+ * 16-byte aligned buffers, 1 <= stride <= 8, R, S <= 32 and pad < 128; other
+ * problems take the plain-load producer.
  */
 TP_API int tp_conv2d_fprop_bf16(const void* x_nhwc, const void* w_krsc, void* y_nhwk, int64_t N, int64_t H, int64_t W,
                          int64_t C, int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad, void* stream);
@@ -201,6 +207,7 @@ TP_API int tp_last_plan(tp_plan* plan);
 /* One compiled mainloop variant. */
 typedef struct {
     int atom, pipe_depth, tile_n, out_f32, conv, smem_bytes;
+    int ldg; /* 1: plain-load producer */
 } tp_kernel_desc;
 
 /* Writes up to cap compiled variants to out (may be NULL) and returns how

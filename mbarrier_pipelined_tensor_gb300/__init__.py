@@ -37,6 +37,7 @@ TP_PATH_MAINLOOP = 1
 TP_PATH_ZERO_FILL = 2
 TP_PATH_TMA_COPY = 3
 TP_PATH_VEC_COPY = 4
+TP_PATH_FALLBACK_MAINLOOP = 5
 
 
 class tp_gemm_opts(ctypes.Structure):
@@ -61,7 +62,8 @@ class tp_plan(ctypes.Structure):
 
 class tp_kernel_desc(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("out_f32", ctypes.c_int), ("conv", ctypes.c_int), ("smem_bytes", ctypes.c_int)]
+                ("out_f32", ctypes.c_int), ("conv", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+                ("ldg", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

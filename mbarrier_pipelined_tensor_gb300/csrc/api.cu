@@ -18,6 +18,7 @@ namespace tp {
 const KernelEntry* table_mainloop_cg1(int* n);
 const KernelEntry* table_mainloop_cg2(int* n);
 const KernelEntry* table_mainloop_conv(int* n);
+const KernelEntry* table_mainloop_fallback(int* n);
 cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensorMap& d, const CopyParams& p,
                                 int grid, cudaStream_t st);
 int copy_smem_bytes(int stages, uint32_t tile_bytes);
@@ -89,11 +90,15 @@ uint64_t wait_limit_ns()
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
 // ------------------------------------------------------ variant table ---
 
+constexpr int kTables = 4;
+
 struct Tables {
-    const KernelEntry* t[3];
-    int n[3];
+    const KernelEntry* t[kTables];
+    int n[kTables];
 };
 
 const Tables& tables()
@@ -103,6 +108,7 @@ const Tables& tables()
         x.t[0] = table_mainloop_cg1(&x.n[0]);
         x.t[1] = table_mainloop_cg2(&x.n[1]);
         x.t[2] = table_mainloop_conv(&x.n[2]);
+        x.t[3] = table_mainloop_fallback(&x.n[3]);
         return x;
     }();
     return tb;
@@ -111,11 +117,11 @@ const Tables& tables()
 const KernelEntry* find_kernel(const KernelKey& k)
 {
     const Tables& tb = tables();
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < kTables; ++i)
         for (int j = 0; j < tb.n[i]; ++j) {
             const KernelKey& e = tb.t[i][j].key;
             if (e.cta_group == k.cta_group && e.bn == k.bn && e.stages == k.stages && e.out_f32 == k.out_f32 &&
-                e.conv == k.conv)
+                e.conv == k.conv && e.ldg == k.ldg)
                 return &tb.t[i][j];
         }
     return nullptr;
@@ -137,23 +143,57 @@ int deepest_fitting(int atom, int tile_n)
     return d;
 }
 
-int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// Picks the (atom, MMA N) not fixed by the caller: the variant with the
+// least estimated time, waves x tile_n / eff, where waves counts rounds of
+// output tiles over the persistent clusters and eff is the variant's
+// measured throughput on a large square GEMM relative to the best one
+// (2-SM, N = 256 at its deepest ring). A fixed field (*atom or *tile_n
+// nonzero) restricts the candidates.
+void choose_variant(int64_t M, int64_t N, int sm_count, int* atom, int* tile_n)
+{
+    struct Cand {
+        int atom, tile_n;
+        double eff;
+    };
+    static const Cand kCands[] = {{2, 256, 1.00}, {1, 256, 0.91}, {2, 128, 0.89}, {1, 128, 0.76}};
+    double best = 0;
+    Cand pick = kCands[0];
+    bool have = false;
+    for (const Cand& c : kCands) {
+        if ((*atom && c.atom != *atom) || (*tile_n && c.tile_n != *tile_n)) continue;
+        const int64_t tiles = cdiv(M, 128 * c.atom) * cdiv(N, c.tile_n);
+        const int64_t clusters = std::max<int64_t>(1, sm_count / c.atom);
+        const double cost = static_cast<double>(cdiv(tiles, clusters)) * c.tile_n / c.eff;
+        if (!have || cost < best) {
+            best = cost;
+            pick = c;
+            have = true;
+        }
+    }
+    *atom = pick.atom;
+    *tile_n = pick.tile_n;
+}
 
 // Variant and launch shape for a GEMM view M x N x K (k_blocks given).
-int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv, const tp_gemm_opts* o,
+int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv, int ldg, const tp_gemm_opts* o,
                   int sm_count, tp_plan* pl)
 {
     int atom = o && o->atom ? o->atom : 0;
     int tile_n = o && o->tile_n ? o->tile_n : 0;
     if (atom != 0 && atom != 1 && atom != 2) return TP_ERR_INVALID_ARG;
     if (tile_n != 0 && tile_n != 128 && tile_n != 256) return TP_ERR_INVALID_ARG;
-    if (atom == 0) atom = 1;
-    if (tile_n == 0) tile_n = 128;
+    if (ldg) {
+        // The plain-load producer exists for the 1-SM atom at N = 128 only.
+        if ((atom && atom != 1) || (tile_n && tile_n != 128)) return TP_ERR_UNSUPPORTED;
+        atom = 1;
+        tile_n = 128;
+    }
+    if (atom == 0 || tile_n == 0) choose_variant(M, N, sm_count, &atom, &tile_n);
     int depth = o && o->pipe_depth ? o->pipe_depth : deepest_fitting(atom, tile_n);
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
     const int64_t smem = mainloop_smem(atom, depth, tile_n);
     if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
-    const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv});
+    const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv, ldg});
     if (!k) return TP_ERR_UNSUPPORTED;
 
     const int64_t m_tiles = cdiv(M, 128 * atom);
@@ -165,7 +205,7 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     if (clusters > tiles) clusters = tiles;
     if (clusters < 1) clusters = 1;
 
-    pl->path = TP_PATH_MAINLOOP;
+    pl->path = ldg ? TP_PATH_FALLBACK_MAINLOOP : TP_PATH_MAINLOOP;
     pl->atom = atom;
     pl->pipe_depth = depth;
     pl->tile_n = tile_n;
@@ -202,15 +242,23 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
         return TP_OK;
     }
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TP_ERR_UNSUPPORTED;
-    // TMA suitability: 16-byte aligned bases and byte pitches.
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda * 2) % 16 || (ldb * 2) % 16 || (ldc * eb) % 16)
-        return TP_ERR_UNSUPPORTED;
-    return plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, opts, sm_count, pl);
+    // Elements must at least be naturally aligned.
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u ||
+        reinterpret_cast<uintptr_t>(C) % eb)
+        return TP_ERR_INVALID_ARG;
+    // TMA suitability: 16-byte aligned bases and byte pitches; otherwise the
+    // plain-load producer feeds the same mainloop.
+    const int ldg = (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda * 2) % 16 || (ldb * 2) % 16 ||
+                     (ldc * eb) % 16)
+                        ? 1
+                        : 0;
+    return plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl);
 }
 
 int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
 {
-    const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv});
+    const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv,
+                                                 pl.path == TP_PATH_FALLBACK_MAINLOOP ? 1 : 0});
     if (!k) return TP_ERR_UNSUPPORTED;
     L.grid = pl.grid;
     L.stream = st;
@@ -261,12 +309,12 @@ int tp_list_kernels(tp_kernel_desc* out, int cap)
 {
     const Tables& tb = tables();
     int n = 0;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < kTables; ++i)
         for (int j = 0; j < tb.n[i]; ++j, ++n) {
             if (out && n < cap) {
                 const KernelEntry& e = tb.t[i][j];
                 out[n] = tp_kernel_desc{e.key.cta_group, e.key.stages, e.key.bn, e.key.out_f32, e.key.conv,
-                                        e.smem_bytes};
+                                        e.smem_bytes, e.key.ldg};
             }
         }
     return n;
@@ -307,22 +355,32 @@ int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
     }
     const int cg = pl.atom;
     const int b_rows = pl.tile_n / cg;
+    const bool ldg = pl.path == TP_PATH_FALLBACK_MAINLOOP;
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
+    const uint32_t eb = out_f32 ? 4 : 2;
+    // TMA stores write whole 16-byte granules of a row: the C map ends at the
+    // last full granule, the epilogue stores the rest (all of C when the
+    // plain-load path runs).
+    const int64_t n_tma = ldg ? 0 : N / (16 / eb) * (16 / eb);
+    if (!ldg) {
     TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
                  {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
                  {64, 128}, CU_TENSOR_MAP_SWIZZLE_128B};
     TiledDesc db{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B),
                  {static_cast<uint64_t>(K), static_cast<uint64_t>(N)}, {static_cast<uint64_t>(ldb) * 2},
                  {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
-    const uint32_t eb = out_f32 ? 4 : 2;
-    const int64_t n_tma = N / (16 / eb) * (16 / eb);
     TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
                  {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
                  {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
     if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db)) || (st = encode_tiled(&L.mapC, dc)))
         return st;
+    }
     GemmParams& p = L.params;
+    p.A = static_cast<const uint16_t*>(A);
+    p.B = static_cast<const uint16_t*>(B);
+    p.lda = lda;
+    p.ldb = ldb;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -377,18 +435,27 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
         t_last_plan = pl;
         return e == cudaSuccess ? TP_OK : cuda_fail(e);
     }
-    // im2col TMA limits (cuTensorMapEncodeIm2col: rank-4 corners in
-    // [-128, 127], traversal strides <= 8) and 16-byte byte strides.
-    if (C % 8 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(y) || stride > 8 || R > 32 || S > 32 ||
-        pad > 127 || M > INT32_MAX || N * H * W > INT32_MAX)
+    const int eb_out = out_f32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w)) & 1u ||
+        reinterpret_cast<uintptr_t>(y) % eb_out)
+        return TP_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N * H * W > INT32_MAX || R * S > INT32_MAX / 64 || K > INT32_MAX)
         return TP_ERR_UNSUPPORTED;
+    // im2col TMA limits (cuTensorMapEncodeIm2col: rank-4 corners in
+    // [-128, 127], traversal strides <= 8) and 16-byte byte strides;
+    // otherwise the plain-load producer gathers the same tiles.
+    const int ldg = (C % 8 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(y) || stride > 8 || R > 32 ||
+                     S > 32 || pad > 127)
+                        ? 1
+                        : 0;
     const int64_t cblocks = cdiv(C, 64);
-    st = plan_mainloop(M, K, R * S * cblocks, out_f32, 1, opts, dev->sm_count, &pl);
+    st = plan_mainloop(M, K, R * S * cblocks, out_f32, 1, ldg, opts, dev->sm_count, &pl);
     if (st) return st;
     const int cg = pl.atom;
     const int b_rows = pl.tile_n / cg;
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
+    if (!ldg) {
     Im2colDesc dx{};
     dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     dx.base = const_cast<void*>(x);
@@ -423,7 +490,14 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
                  {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
     if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw)) || (st = encode_tiled(&L.mapC, dy)))
         return st;
+    }
     GemmParams& p = L.params;
+    p.A = static_cast<const uint16_t*>(x);
+    p.B = static_cast<const uint16_t*>(w);
+    p.conv_H = static_cast<int>(H);
+    p.conv_W = static_cast<int>(W);
+    p.conv_C = static_cast<int>(C);
+    p.conv_R = static_cast<int>(R);
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(K);
     p.K = static_cast<int>(R * S * C);
@@ -437,9 +511,9 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.conv_pad = static_cast<int>(pad);
     p.conv_S = static_cast<int>(S);
     p.conv_cblocks = static_cast<int>(cblocks);
-    p.n_tma = static_cast<int>(K);  // K % 8 == 0: rows are whole 16-byte granules
+    p.n_tma = ldg ? 0 : static_cast<int>(K);  // TMA path: K % 8 == 0, rows are whole 16-byte granules
     p.C = y;
-    p.ldc_bytes = K * eb;
+    p.ldc_bytes = K * eb_out;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};
     st = launch_plan(pl, L, s);
     if (st == TP_OK) t_last_plan = pl;

@@ -98,6 +98,12 @@ struct GemmParams {
     int group_m;   // tile raster: group_m M-tiles share a sweep over N
     // convolution only
     int conv_P, conv_Q, conv_stride, conv_pad, conv_S, conv_cblocks;
+    // plain-load producer only (operands TMA cannot describe): A / B (or x /
+    // w) with their pitches in elements, and the conv input extents
+    const uint16_t* A;
+    const uint16_t* B;
+    int64_t lda, ldb;
+    int conv_H, conv_W, conv_C, conv_R;
     WaitCtl wait;
 };
 
@@ -115,6 +121,7 @@ struct KernelKey {
     int stages;     // PIPE_DEPTH
     int out_f32;
     int conv;
+    int ldg;        // 1: plain-load producer instead of TMA
 };
 
 struct GemmLaunch {

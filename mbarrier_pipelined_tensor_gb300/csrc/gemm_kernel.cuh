@@ -21,6 +21,14 @@
 // ring run without waiting. Two TMEM accumulators let the epilogue of tile
 // t-1 overlap the mainloop of tile t (the "store k-1" of the steady state).
 //
+// Plain-load producer (LDG = true, 1-SM only): for operands TMA cannot
+// describe ("B200 Tma Pipeline Designer", step 1: keep the vectorized thread
+// copy), all 32 lanes of warp 0 gather the stage with global loads, bounds
+// checked element by element, and write it in the same 128-byte-swizzled
+// layout TMA would produce; each lane fences its generic-proxy writes for the
+// tensor core's async-proxy reads, and one lane makes the stage's single
+// arrival. The epilogue then writes C with plain stores.
+//
 // Atoms ("two-free-pipeline-stages" note): CG = 1 is the 1-SM atom (each CTA
 // owns a 128 x BN tile and holds all of its B tile); CG = 2 is the 2-SM atom
 // (a CTA pair owns 256 x BN, the leader issues cta_group::2 MMAs, and each
@@ -85,13 +93,79 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+// 8 consecutive bf16 (one 16-byte chunk of a swizzle row) gathered with
+// bounds checks; out-of-range elements are zero, as TMA's fill would be.
+__device__ __forceinline__ void gather8(const uint16_t* __restrict__ row_ptr, bool row_ok, int col0, int cols,
+                                        uint32_t (&v)[4])
+{
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int c = col0 + 2 * e;
+        const uint32_t lo = (row_ok && c < cols) ? row_ptr[c] : 0u;
+        const uint32_t hi = (row_ok && c + 1 < cols) ? row_ptr[c + 1] : 0u;
+        v[e] = lo | (hi << 16);
+    }
+}
+
+// Fills one stage (A: 128 rows, B: B_ROWS rows, 64 bf16 each) with plain
+// loads; lane L handles chunks L, L+32, ... (8 chunks per 128-byte row).
+template <int B_ROWS, bool CONV>
+__device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA, uint32_t dB, int m_row, int n_row,
+                                               int kb, uint32_t lane)
+{
+    int r = 0, sx = 0, c0 = kb * 64;
+    if constexpr (CONV) {
+        const int rs = kb / p.conv_cblocks;
+        c0 = (kb - rs * p.conv_cblocks) * 64;
+        r = rs / p.conv_S;
+        sx = rs - r * p.conv_S;
+    }
+    for (int idx = static_cast<int>(lane); idx < 128 * 8; idx += 32) {
+        const int row = idx >> 3, j = idx & 7;
+        const int m = m_row + row;
+        uint32_t v[4];
+        if constexpr (CONV) {
+            const int pq = p.conv_P * p.conv_Q;
+            const int img = m / pq;
+            const int rem = m - img * pq;
+            const int pp = rem / p.conv_Q;
+            const int qq = rem - pp * p.conv_Q;
+            const int h = pp * p.conv_stride - p.conv_pad + r;
+            const int w = qq * p.conv_stride - p.conv_pad + sx;
+            const bool ok = m < p.M && h >= 0 && h < p.conv_H && w >= 0 && w < p.conv_W;
+            const uint16_t* rp = p.A + ((static_cast<int64_t>(img) * p.conv_H + (ok ? h : 0)) * p.conv_W +
+                                        (ok ? w : 0)) * p.conv_C;
+            gather8(rp, ok, c0 + j * 8, p.conv_C, v);
+        } else {
+            const bool ok = m < p.M;
+            gather8(p.A + static_cast<int64_t>(ok ? m : 0) * p.lda, ok, c0 + j * 8, p.K, v);
+        }
+        st_shared_v4(dA + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
+    }
+    for (int idx = static_cast<int>(lane); idx < B_ROWS * 8; idx += 32) {
+        const int row = idx >> 3, j = idx & 7;
+        const int n = n_row + row;
+        const bool ok = n < p.N;
+        uint32_t v[4];
+        if constexpr (CONV) {
+            const uint16_t* rp =
+                p.B + ((static_cast<int64_t>(ok ? n : 0) * p.conv_R + r) * p.conv_S + sx) * p.conv_C;
+            gather8(rp, ok, c0 + j * 8, p.conv_C, v);
+        } else {
+            gather8(p.B + static_cast<int64_t>(ok ? n : 0) * p.ldb, ok, c0 + j * 8, p.K, v);
+        }
+        st_shared_v4(dB + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
+    }
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
 __global__ void __launch_bounds__(192, 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const GemmParams p)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
     constexpr bool CL = (CG == 2);
+    static_assert(!LDG || CG == 1, "the plain-load producer feeds the 1-SM atom");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -128,9 +202,11 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
-        prefetch_tensormap(&mapA);
-        prefetch_tensormap(&mapB);
-        prefetch_tensormap(&mapC);
+        if constexpr (!LDG) {
+            prefetch_tensormap(&mapA);
+            prefetch_tensormap(&mapB);
+            prefetch_tensormap(&mapC);
+        }
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -145,7 +221,35 @@ __global__ void __launch_bounds__(192, 1)
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
-    if (warp == 0) {
+    if (LDG && warp == 0) {
+        // ------------------------------------- plain-load producer ---
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+            int mt, nt;
+            tile_coords(t, p, mt, nt);
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                int free_ok = 1;
+                if (lane == 0)
+                    free_ok = wait_bounded<false>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
+                if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                ldg_fill_stage<Cfg::B_ROWS, CONV>(p, sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES, mt * Cfg::BM,
+                                                  nt * BN, kb, lane);
+                fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_bar(s));
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
         // --------------------------------------------------- producer ---
         if (elect_one()) {
             int s = 0;
@@ -387,11 +491,11 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
 cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
-    auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV>;
+    auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -409,11 +513,11 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.params);
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
 constexpr KernelEntry mainloop_entry()
 {
-    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0},
-                       &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV>,
+    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0},
+                       &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG>,
                        MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES};
 }
 

@@ -1,0 +1,21 @@
+// Plain-load producer variants of the mainloop (operands TMA cannot
+// describe): 1-SM atom, MMA N = 128, deepest ring, GEMM and conv, bf16 and
+// fp32 outputs.
+#include "gemm_kernel.cuh"
+
+namespace tp {
+
+static const KernelEntry k_table[] = {
+    mainloop_entry<1, 128, 6, false, false, true>(),
+    mainloop_entry<1, 128, 6, true, false, true>(),
+    mainloop_entry<1, 128, 6, false, true, true>(),
+    mainloop_entry<1, 128, 6, true, true, true>(),
+};
+
+const KernelEntry* table_mainloop_fallback(int* n)
+{
+    *n = static_cast<int>(sizeof(k_table) / sizeof(k_table[0]));
+    return k_table;
+}
+
+}  // namespace tp

@@ -204,10 +204,66 @@ def test_gemm_persistent_many_tiles_small_grid():
     M, N, K = 1024, 1024, 320
     A, B = datagen.gemm_operands(M, N, K, seed=41)
     for tile_n in (128, 256):
-        got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, tile_n=tile_n, max_ctas=3, group_m=3)
+        got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=1, tile_n=tile_n, max_ctas=3, group_m=3)
         assert plan["grid"] == 3
         ref, ab = oracle.gemm(A, B, M, N, K, K, K)
         check_against_oracle(got, ref, ab, True, f"persistent n{tile_n}")
+
+
+# ---------------------------------------------- plain-load producer ---
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,offs", [
+    (300, 200, 448, 449, 450, 201, (1, 3, 5)),     # odd pitches, misaligned bases
+    (129, 77, 1000, 1003, 1001, 77, (0, 0, 1)),
+    (520, 600, 1216, 1216, 1216, 600, (4, 0, 0)),  # only A misaligned (by 8 bytes)
+])
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_gemm_fallback_producer(M, N, K, lda, ldb, ldc, offs, out_f32):
+    A, B = datagen.gemm_operands(M, N, K, seed=51, lda=lda, ldb=ldb)
+    oa, ob, oc = offs
+    a_all = dev_bf16(np.concatenate([np.zeros(oa, np.uint16), A.reshape(-1)]))
+    b_all = dev_bf16(np.concatenate([np.zeros(ob, np.uint16), B.reshape(-1)]))
+    c_all = new_out(1, M * ldc + oc, out_f32).reshape(-1)
+    a, b, c = a_all[oa:], b_all[ob:], c_all[oc:]
+    tp.tp_gemm_bf16_ex(a, b, c, M, N, K, lda, ldb, ldc, out_f32=out_f32)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    full = host_f64(c_all)
+    assert np.all(np.isnan(full[:oc]))
+    got = full[oc:].reshape(M, ldc)
+    assert np.all(np.isnan(got[:, N:]))
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    check_against_oracle(got[:, :N], ref, ab, out_f32, "fallback producer")
+
+
+@pytest.mark.parametrize("case", [(2, 9, 7, 3, 20, 3, 3, 1, 1), (1, 12, 11, 70, 66, 3, 3, 2, 1),
+                                  (2, 6, 6, 12, 8, 1, 1, 1, 0)])
+def test_conv_fallback_producer(case):
+    # C or K not a multiple of 8: the im2col tiles are gathered with plain loads.
+    N, H, W, C, K, R, S, st, pad = case
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=52)
+    P, Q = oracle.conv_out_hw(H, W, R, S, st, pad)
+    y = new_out(N * P * Q, K, True)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, st, pad, out_f32=True)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, st, pad)
+    check_against_oracle(host_f64(y), ref, ab, True, f"conv fallback {case}")
+
+
+def test_fallback_matches_tma_path_bit_for_bit():
+    # The same operands through both producers: the tensor core sees the same
+    # swizzled stages, so the outputs are identical.
+    M, N, K = 384, 256, 640
+    A, B = datagen.gemm_operands(M, N, K, seed=53)
+    a, b = dev_bf16(A), dev_bf16(B)
+    b_off_all = dev_bf16(np.concatenate([np.zeros(1, np.uint16), B.reshape(-1)]))
+    c1, c2 = new_out(M, N, True), new_out(M, N, True)
+    tp.tp_gemm_bf16_ex(a, b, c1, M, N, K, K, K, N, out_f32=True, atom=1, tile_n=128, pipe_depth=6)
+    tp.tp_gemm_bf16_ex(a, b_off_all[1:], c2, M, N, K, K, K, N, out_f32=True)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    assert torch.equal(c1, c2)
 
 
 # ------------------------------------------------------------------ conv ---

@@ -113,10 +113,26 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, A=AL, B=AL, C=AL, out_f32=False,
 
 
 def test_plan_ragged_small_config():
-    st, p = plan(320, 200, 448)
+    st, p = plan(320, 200, 448, atom=1, tile_n=128)
     assert st == tp.TP_OK and p["path"] == tp.TP_PATH_MAINLOOP
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (3, 2, 7)
     assert p["grid"] == 6 and p["smem_bytes"] <= SMEM_LIMIT
+    st, p = plan(320, 200, 448, atom=2, tile_n=128)
+    assert (p["m_tiles"], p["n_tiles"], p["grid"], p["cluster"]) == (2, 2, 8, 2)
+
+
+def test_auto_variant_choice():
+    # Large square: the 2-SM atom at MMA N = 256 (fewest waves x widest tile).
+    st, p = plan(8192, 8192, 8192)
+    assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (2, 256, 6)
+    # Few output tiles: N = 128 tiles spread the work over more SMs.
+    st, p = plan(1000, 1000, 1000, lda=1008, ldb=1008, ldc=1000, out_f32=True)
+    assert (p["atom"], p["tile_n"]) == (2, 128) and p["grid"] == 64
+    # A fixed field restricts the choice.
+    st, p = plan(8192, 8192, 8192, atom=1)
+    assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 256, 4)
+    st, p = plan(8192, 8192, 8192, tile_n=128)
+    assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (2, 128, 8)
 
 
 def test_plan_big_square_grid_is_persistent():
@@ -144,10 +160,16 @@ def test_plan_edge_cases():
 
 
 def test_plan_tma_suitability():
-    assert plan(64, 64, 64, A=AL + 2)[0] == tp.TP_ERR_UNSUPPORTED     # base not 16-B aligned
-    assert plan(64, 64, 60, lda=60)[0] == tp.TP_ERR_UNSUPPORTED       # lda*2 = 120 not a multiple of 16
-    assert plan(64, 60, 64, ldc=60, out_f32=True)[0] == tp.TP_OK      # 60*4 = 240 = 15*16
-    assert plan(64, 60, 64, ldc=60)[0] == tp.TP_ERR_UNSUPPORTED       # 60*2 = 120
+    FB, ML = tp.TP_PATH_FALLBACK_MAINLOOP, tp.TP_PATH_MAINLOOP
+    assert plan(64, 64, 64, A=AL + 2)[1]["path"] == FB                # base not 16-B aligned
+    assert plan(64, 64, 60, lda=60)[1]["path"] == FB                  # lda*2 = 120 not a multiple of 16
+    assert plan(64, 60, 64, ldc=60, out_f32=True)[1]["path"] == ML    # 60*4 = 240 = 15*16
+    assert plan(64, 60, 64, ldc=60)[1]["path"] == FB                  # 60*2 = 120
+    st, p = plan(64, 64, 64, A=AL + 2)
+    assert st == tp.TP_OK and (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 128, 6)
+    assert plan(64, 64, 64, A=AL + 1)[0] == tp.TP_ERR_INVALID_ARG     # a bf16 must be 2-byte aligned
+    assert plan(64, 64, 64, C=AL + 2, out_f32=True)[0] == tp.TP_ERR_INVALID_ARG
+    assert plan(64, 64, 64, A=AL + 2, atom=2)[0] == tp.TP_ERR_UNSUPPORTED
 
 
 def test_plan_budget_errors():
