@@ -51,6 +51,10 @@ def parse_args():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--depth", type=int, default=0)
     ap.add_argument("--size", type=int, default=8192, help="M = N = K of the timed GEMM")
+    ap.add_argument("--group-m", type=int, default=0, help="tile raster group (0 = library default)")
+    ap.add_argument("--l2-hint", type=int, default=0, help="operand L2 priorities (tp_gemm_opts.l2_hint)")
+    ap.add_argument("--gsweep", type=str, default="",
+                    help="comma-separated group_m[:l2_hint] values: time a --steps loop of each")
     return ap.parse_args()
 
 
@@ -266,10 +270,23 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         byts = 2.0 * (Ms * Ks + Ns * Ks + Ms * Ns)
         tfl = f / (med * 1e-3) / 1e12
         bound = min(peaks["bf16_tflops"], f / byts * peaks["hbm_gbs"] * 1e9 / 1e12)
-        sk[f"{Ms}x{Ns}x{Ks}"] = {"us": round(med * 1e3, 2), "tflops": round(tfl, 1),
-                                 "roofline_tflops": round(bound, 1), "frac": round(tfl / bound, 3),
-                                 "grid": tp.tp_last_plan()["grid"]}
-        del a, b, c
+        row = {"us": round(med * 1e3, 2), "tflops": round(tfl, 1), "roofline_tflops": round(bound, 1),
+               "frac": round(tfl / bound, 3), "grid": tp.tp_last_plan()["grid"]}
+        # split-K with a caller workspace (slices chosen by the library)
+        ws = torch.empty(tp.tp_gemm_splitk_workspace_bytes(Ms, Ns, 16) // 4, dtype=torch.float32, device="cuda")
+
+        def gs():
+            tp.tp_gemm_bf16_splitk(a, b, c, Ms, Ns, Ks, Ks, Ks, Ns, splits=0, workspace=ws, stream=s)
+
+        for _ in range(3):
+            gs()
+        med_s, _ = time_each_flushed(torch, stream, gs, 20, flush_buf)
+        pl = tp.tp_last_plan()
+        tfl_s = f / (med_s * 1e-3) / 1e12
+        row["splitk"] = {"us": round(med_s * 1e3, 2), "tflops": round(tfl_s, 1), "frac": round(tfl_s / bound, 3),
+                         "splits": pl["splits"], "grid": pl["grid"], "atom": pl["atom"], "tile_n": pl["tile_n"]}
+        sk[f"{Ms}x{Ns}x{Ks}"] = row
+        del a, b, c, ws
     rows["skinny_gemm_set"] = {"unit": "TFLOP/s", "l2": "flushed between calls", **sk}
 
     # small ragged GEMM 320x200x448 (latency)
@@ -389,7 +406,25 @@ def tp_arm(args):
     c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
-    opts = {k: v for k, v in (("atom", args.atom), ("tile_n", args.tile_n), ("pipe_depth", args.depth)) if v}
+    opts = {k: v for k, v in (("atom", args.atom), ("tile_n", args.tile_n), ("pipe_depth", args.depth),
+                              ("group_m", args.group_m), ("l2_hint", args.l2_hint)) if v}
+    if args.gsweep:
+        out = []
+        for item in args.gsweep.split(","):
+            g, _, h = item.partition(":")
+            g, h = int(g), int(h or 0)
+            o = dict(opts, group_m=g, l2_hint=h)
+            fn = lambda: tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, stream=s, **o)  # noqa: E731
+            for _ in range(5):
+                fn()
+            sampler = ClockSampler(local).start()
+            ms = time_loop(torch, stream, fn, args.steps)
+            clk = sampler.stop()
+            out.append({"group_m": g, "l2_hint": h, "tflops": round(2.0 * M * N * K * args.steps / (ms * 1e-3) / 1e12, 1),
+                        "ms_per_launch": round(ms / args.steps, 4), "sm_mhz": clk["sm_mhz"],
+                        "reasons": clk["reasons"]})
+        print(json.dumps({"gsweep": out, "size": M, "steps": args.steps}), flush=True)
+        return 0
 
     def step():
         tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, stream=s, **opts)

@@ -89,6 +89,9 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   tile_n:     MMA N (128 or 256).
  *   group_m:    tile raster: group_m M-tiles share one sweep over N.
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM).
+ *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
+ *               1 none, 2 A evict-last / B evict-first, 3 A evict-last,
+ *               4 B evict-first.
  * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
  * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
  * "StageCount<9> fails the capacity assert"; a combination that fits but is
@@ -100,12 +103,40 @@ typedef struct {
     int tile_n;
     int group_m;
     int max_ctas;
+    int l2_hint;
 } tp_gemm_opts;
 
 /* tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit choices (opts may be NULL).
  * out_f32 selects a float C (1) or a bf16 C (0). */
 TP_API int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                     int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, void* stream);
+
+/*
+ * Split-K GEMM for problems with few output tiles (skinny M or N, deep K):
+ * each (output tile, K slice) work unit runs the same mainloop and writes its
+ * fp32 partial sum into slice `s` of a caller-provided workspace; a second
+ * kernel adds the slices in order (fp32) and writes C (bf16 RNE or fp32).
+ * Results equal C = A . B within the fp32 accumulator's error bound; the
+ * summation order differs from tp_gemm_bf16's.
+ *   splits:    K slices (1..k_blocks, k_blocks = ceil(K/64)); 0 chooses a
+ *              count that fills the GPU, capped by what the workspace holds.
+ *              Slice counts are adjusted down so that none is empty.
+ *   workspace: caller-owned device memory, 16-byte aligned, at least
+ *              tp_gemm_splitk_workspace_bytes(M, N, splits) bytes; the call
+ *              overwrites it. Calls that overlap on the GPU must not share a
+ *              workspace. With one slice it is not touched (may be NULL).
+ * A and B must be TMA-describable (16-byte aligned, lda*2 and ldb*2 multiples
+ * of 16), else TP_ERR_UNSUPPORTED; C needs only natural alignment. A
+ * workspace that is too small for an explicit `splits` returns
+ * TP_ERR_INVALID_ARG. Two kernels are launched on `stream`.
+ */
+TP_API int tp_gemm_bf16_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc, int out_f32, int splits, void* workspace,
+                               int64_t workspace_bytes, const tp_gemm_opts* opts, void* stream);
+
+/* Workspace bytes tp_gemm_bf16_splitk needs for `splits` slices:
+ * splits x M x round_up(N, 4) x 4. Host-only. */
+TP_API int tp_gemm_splitk_workspace_bytes(int64_t M, int64_t N, int splits, int64_t* bytes);
 
 /*
  * Forward convolution as an implicit GEMM on the same mainloop; the A tile is
@@ -190,6 +221,7 @@ typedef struct {
     int cluster;     /* CTAs per cluster */
     int smem_bytes;  /* dynamic shared memory per CTA */
     int64_t m_tiles, n_tiles, k_blocks;
+    int splits;      /* K slices (1 unless split-K ran) */
 } tp_plan;
 
 /*
@@ -207,7 +239,8 @@ TP_API int tp_last_plan(tp_plan* plan);
 /* One compiled mainloop variant. */
 typedef struct {
     int atom, pipe_depth, tile_n, out_f32, conv, smem_bytes;
-    int ldg; /* 1: plain-load producer */
+    int ldg;    /* 1: plain-load producer */
+    int splitk; /* 1: split-K partials into a workspace */
 } tp_kernel_desc;
 
 /* Writes up to cap compiled variants to out (may be NULL) and returns how

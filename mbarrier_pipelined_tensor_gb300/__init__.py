@@ -42,7 +42,7 @@ TP_PATH_FALLBACK_MAINLOOP = 5
 
 class tp_gemm_opts(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+                ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int), ("l2_hint", ctypes.c_int)]
 
 
 class tp_copy_opts(ctypes.Structure):
@@ -54,7 +54,8 @@ class tp_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int),
                 ("tile_n", ctypes.c_int), ("out_f32", ctypes.c_int), ("conv", ctypes.c_int),
                 ("grid", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64)]
+                ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
+                ("splits", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -63,7 +64,7 @@ class tp_plan(ctypes.Structure):
 class tp_kernel_desc(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("out_f32", ctypes.c_int), ("conv", ctypes.c_int), ("smem_bytes", ctypes.c_int),
-                ("ldg", ctypes.c_int)]
+                ("ldg", ctypes.c_int), ("splitk", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -74,6 +75,8 @@ _SIGS = {
     "tp_gemm_bf16": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
     "tp_gemm_bf16_f32": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
     "tp_gemm_bf16_ex": ([_P, _P, _P] + [_I64] * 6 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
+    "tp_gemm_bf16_splitk": ([_P, _P, _P] + [_I64] * 6 + [_I, _I, _P, _I64, ctypes.POINTER(tp_gemm_opts), _P], _I),
+    "tp_gemm_splitk_workspace_bytes": ([_I64, _I64, _I, ctypes.POINTER(_I64)], _I),
     "tp_conv2d_fprop_bf16": ([_P, _P, _P] + [_I64] * 9 + [_P], _I),
     "tp_conv2d_fprop_bf16_ex": ([_P, _P, _P] + [_I64] * 9 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_tma_copy_2d": ([_P, _P, _I64, _I64, _I64, _P], _I),
@@ -147,14 +150,30 @@ def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
            "tp_gemm_bf16_f32")
 
 
-def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0):
-    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas)
+def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0):
+    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint)
 
 
 def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):
     o = _opts(**opts)
     _check(_lib.tp_gemm_bf16_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, int(bool(out_f32)),
                                 ctypes.byref(o), _stream(stream)), "tp_gemm_bf16_ex")
+
+
+def tp_gemm_bf16_splitk(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, splits=0, workspace=None,
+                        workspace_bytes=0, stream=None, **opts):
+    o = _opts(**opts)
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.tp_gemm_bf16_splitk(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, int(bool(out_f32)),
+                                    splits, _ptr(workspace), workspace_bytes, ctypes.byref(o), _stream(stream)),
+           "tp_gemm_bf16_splitk")
+
+
+def tp_gemm_splitk_workspace_bytes(M, N, splits) -> int:
+    b = _I64()
+    _check(_lib.tp_gemm_splitk_workspace_bytes(M, N, splits, ctypes.byref(b)), "tp_gemm_splitk_workspace_bytes")
+    return int(b.value)
 
 
 def tp_conv2d_fprop_bf16(x, w, y, N, H, W, C, K, R, S, stride, pad, stream=None):

@@ -19,6 +19,9 @@ const KernelEntry* table_mainloop_cg1(int* n);
 const KernelEntry* table_mainloop_cg2(int* n);
 const KernelEntry* table_mainloop_conv(int* n);
 const KernelEntry* table_mainloop_fallback(int* n);
+const KernelEntry* table_mainloop_splitk(int* n);
+cudaError_t launch_splitk_reduce(const float* ws, void* C, int M, int N, int64_t ldw, int64_t ldc, int splits,
+                                 int out_f32, int sm_count, cudaStream_t st);
 cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensorMap& d, const CopyParams& p,
                                 int grid, cudaStream_t st);
 int copy_smem_bytes(int stages, uint32_t tile_bytes);
@@ -94,7 +97,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------ variant table ---
 
-constexpr int kTables = 4;
+constexpr int kTables = 5;
 
 struct Tables {
     const KernelEntry* t[kTables];
@@ -109,6 +112,7 @@ const Tables& tables()
         x.t[1] = table_mainloop_cg2(&x.n[1]);
         x.t[2] = table_mainloop_conv(&x.n[2]);
         x.t[3] = table_mainloop_fallback(&x.n[3]);
+        x.t[4] = table_mainloop_splitk(&x.n[4]);
         return x;
     }();
     return tb;
@@ -121,7 +125,7 @@ const KernelEntry* find_kernel(const KernelKey& k)
         for (int j = 0; j < tb.n[i]; ++j) {
             const KernelKey& e = tb.t[i][j].key;
             if (e.cta_group == k.cta_group && e.bn == k.bn && e.stages == k.stages && e.out_f32 == k.out_f32 &&
-                e.conv == k.conv && e.ldg == k.ldg)
+                e.conv == k.conv && e.ldg == k.ldg && e.splitk == k.splitk)
                 return &tb.t[i][j];
         }
     return nullptr;
@@ -193,7 +197,7 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
     const int64_t smem = mainloop_smem(atom, depth, tile_n);
     if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
-    const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv, ldg});
+    const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv, ldg, 0});
     if (!k) return TP_ERR_UNSUPPORTED;
 
     const int64_t m_tiles = cdiv(M, 128 * atom);
@@ -217,14 +221,60 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     pl->m_tiles = m_tiles;
     pl->n_tiles = n_tiles;
     pl->k_blocks = k_blocks;
+    pl->splits = 1;
     return TP_OK;
 }
 
+// K slices for split-K: the count with the least estimated time,
+// waves x K blocks per slice, plus the partial-sum traffic (each extra slice
+// writes and re-reads one fp32 tile, about two K blocks of operand loads).
+int choose_splits(int64_t tiles, int64_t clusters, int64_t k_blocks)
+{
+    int best_s = 1;
+    double best = 0;
+    for (int s = 1; s <= 16 && s <= k_blocks; ++s) {
+        const int64_t units = tiles * s;
+        const double cost = static_cast<double>(cdiv(units, clusters)) * static_cast<double>(cdiv(k_blocks, s)) +
+                            (s > 1 ? 2.0 * s * static_cast<double>(tiles) / static_cast<double>(clusters) : 0.0);
+        if (s == 1 || cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+// Slices actually used so that none is empty.
+void normalize_splits(int64_t k_blocks, int* splits, int* kb_per_split)
+{
+    int s = *splits < 1 ? 1 : *splits;
+    if (s > k_blocks) s = static_cast<int>(k_blocks);
+    const int kps = static_cast<int>(cdiv(k_blocks, s));
+    *kb_per_split = kps;
+    *splits = static_cast<int>(cdiv(k_blocks, kps));
+}
+
+int64_t splitk_ldw(int64_t N) { return (N + 3) / 4 * 4; }
+
 int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
 {
-    int g = o && o->group_m > 0 ? o->group_m : 16;
+    int g = o && o->group_m > 0 ? o->group_m : 8;
     if (g > m_tiles) g = static_cast<int>(m_tiles);
     return g < 1 ? 1 : g;
+}
+
+// L2 priorities of the A / B loads (0 normal, 1 evict first, 2 evict last).
+void l2_hints_for(const tp_gemm_opts* o, int* a, int* b)
+{
+    const int h = o ? o->l2_hint : 0;
+    *a = 0;
+    *b = 0;
+    switch (h) {
+    case 2: *a = 2; *b = 1; break;
+    case 3: *a = 2; break;
+    case 4: *b = 1; break;
+    default: break;  // 0 (choose) and 1 (none): normal priority
+    }
 }
 
 int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -258,7 +308,8 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
 int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
 {
     const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv,
-                                                 pl.path == TP_PATH_FALLBACK_MAINLOOP ? 1 : 0});
+                                                 pl.path == TP_PATH_FALLBACK_MAINLOOP ? 1 : 0,
+                                                 pl.splits > 1 ? 1 : 0});
     if (!k) return TP_ERR_UNSUPPORTED;
     L.grid = pl.grid;
     L.stream = st;
@@ -314,7 +365,7 @@ int tp_list_kernels(tp_kernel_desc* out, int cap)
             if (out && n < cap) {
                 const KernelEntry& e = tb.t[i][j];
                 out[n] = tp_kernel_desc{e.key.cta_group, e.key.stages, e.key.bn, e.key.out_f32, e.key.conv,
-                                        e.smem_bytes, e.key.ldg};
+                                        e.smem_bytes, e.key.ldg, e.key.splitk};
             }
         }
     return n;
@@ -333,14 +384,22 @@ int tp_gemm_plan(const void* A, const void* B, const void* C, int64_t M, int64_t
     return gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32 ? 1 : 0, opts, sm_count, plan);
 }
 
-int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                    int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, void* stream)
+}  // extern "C"
+
+namespace {
+
+// The GEMM launch shared by the plain and the split-K entry points.
+// splitk: 0 plain; 1 split-K with `splits` slices (0 = choose) into the
+// caller's fp32 workspace, then a reduction into C.
+int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, int out_f32, const tp_gemm_opts* opts, int splitk, int splits, void* ws,
+              int64_t ws_bytes, void* stream)
 {
     out_f32 = out_f32 ? 1 : 0;
     tp_plan pl;
     std::memset(&pl, 0, sizeof(pl));
     t_last_plan = pl;
-    if (M < 0 || N < 0 || K < 0) return TP_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || splits < 0 || ws_bytes < 0) return TP_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return TP_OK;
     DeviceState* dev = nullptr;
     int st = device_state(&dev);
@@ -353,28 +412,62 @@ int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
         t_last_plan = pl;
         return e == cudaSuccess ? TP_OK : cuda_fail(e);
     }
+    const bool ldg = pl.path == TP_PATH_FALLBACK_MAINLOOP;
+    const int64_t ldw = splitk_ldw(N);
+    int kps = static_cast<int>(pl.k_blocks);
+    if (splitk) {
+        // Split-K feeds the mainloop through TMA only.
+        if (ldg) return TP_ERR_UNSUPPORTED;
+        const int64_t slice_bytes = M * ldw * 4;
+        const int64_t cap = (ws && slice_bytes > 0) ? ws_bytes / slice_bytes : 0;
+        const int64_t tiles = pl.m_tiles * pl.n_tiles;
+        const int64_t clusters = std::max<int64_t>(1, (opts && opts->max_ctas > 0 ? opts->max_ctas : dev->sm_count) /
+                                                          pl.atom);
+        int sp = splits > 0 ? splits : choose_splits(tiles, clusters, pl.k_blocks);
+        if (splits == 0 && sp > cap) sp = static_cast<int>(std::max<int64_t>(1, cap));
+        normalize_splits(pl.k_blocks, &sp, &kps);
+        if (sp > 1) {
+            if (sp > cap || (reinterpret_cast<uintptr_t>(ws) & 15u)) return TP_ERR_INVALID_ARG;
+            const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
+            if (!k) return TP_ERR_UNSUPPORTED;
+            pl.splits = sp;
+            int64_t units = tiles * sp;
+            int64_t cl = std::min<int64_t>(clusters, units);
+            pl.grid = static_cast<int>(cl * pl.atom);
+            pl.smem_bytes = k->smem_bytes;
+        }
+    }
+    const bool use_splitk = pl.splits > 1;
     const int cg = pl.atom;
     const int b_rows = pl.tile_n / cg;
-    const bool ldg = pl.path == TP_PATH_FALLBACK_MAINLOOP;
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
     const uint32_t eb = out_f32 ? 4 : 2;
     // TMA stores write whole 16-byte granules of a row: the C map ends at the
     // last full granule, the epilogue stores the rest (all of C when the
-    // plain-load path runs).
-    const int64_t n_tma = ldg ? 0 : N / (16 / eb) * (16 / eb);
+    // plain-load path runs). Split-K partials go to the workspace, whose rows
+    // are whole granules.
+    const int64_t n_tma = use_splitk ? ldw : (ldg ? 0 : N / (16 / eb) * (16 / eb));
     if (!ldg) {
-    TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
-                 {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
-                 {64, 128}, CU_TENSOR_MAP_SWIZZLE_128B};
-    TiledDesc db{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B),
-                 {static_cast<uint64_t>(K), static_cast<uint64_t>(N)}, {static_cast<uint64_t>(ldb) * 2},
-                 {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
-    TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
-                 {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
-                 {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
-    if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db)) || (st = encode_tiled(&L.mapC, dc)))
-        return st;
+        TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
+                     {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
+                     {64, 128}, CU_TENSOR_MAP_SWIZZLE_128B};
+        TiledDesc db{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B),
+                     {static_cast<uint64_t>(K), static_cast<uint64_t>(N)}, {static_cast<uint64_t>(ldb) * 2},
+                     {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
+        if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db))) return st;
+        if (use_splitk) {
+            TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws,
+                         {static_cast<uint64_t>(ldw), static_cast<uint64_t>(M), static_cast<uint64_t>(pl.splits)},
+                         {static_cast<uint64_t>(ldw) * 4, static_cast<uint64_t>(M * ldw) * 4},
+                         {32, 32, 1}, CU_TENSOR_MAP_SWIZZLE_128B};
+            if ((st = encode_tiled(&L.mapC, dw))) return st;
+        } else {
+            TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
+                         {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
+                         {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+            if ((st = encode_tiled(&L.mapC, dc))) return st;
+        }
     }
     GemmParams& p = L.params;
     p.A = static_cast<const uint16_t*>(A);
@@ -387,14 +480,54 @@ int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
     p.m_tiles = static_cast<int>(pl.m_tiles);
     p.n_tiles = static_cast<int>(pl.n_tiles);
     p.k_blocks = static_cast<int>(pl.k_blocks);
+    p.splits = use_splitk ? pl.splits : 1;
+    p.kb_per_split = use_splitk ? kps : p.k_blocks;
     p.group_m = group_m_for(opts, pl.m_tiles);
+    l2_hints_for(opts, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
-    p.C = C;
-    p.ldc_bytes = ldc * eb;
+    p.C = use_splitk ? ws : C;
+    p.ldc_bytes = use_splitk ? ldw * 4 : ldc * eb;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    if (use_splitk) {
+        const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
+        L.grid = pl.grid;
+        L.stream = s;
+        cudaError_t e = k->launch(L);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = launch_splitk_reduce(static_cast<const float*>(ws), C, static_cast<int>(M), static_cast<int>(N), ldw,
+                                 ldc, pl.splits, out_f32, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        pl.out_f32 = out_f32;
+        t_last_plan = pl;
+        return TP_OK;
+    }
     st = launch_plan(pl, L, s);
     if (st == TP_OK) t_last_plan = pl;
     return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                    int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, void* stream)
+{
+    return gemm_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, 0, 0, nullptr, 0, stream);
+}
+
+int tp_gemm_splitk_workspace_bytes(int64_t M, int64_t N, int splits, int64_t* bytes)
+{
+    if (!bytes || M < 0 || N < 0 || splits < 1) return TP_ERR_INVALID_ARG;
+    *bytes = static_cast<int64_t>(splits) * M * splitk_ldw(N) * 4;
+    return TP_OK;
+}
+
+int tp_gemm_bf16_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                        int64_t ldb, int64_t ldc, int out_f32, int splits, void* workspace, int64_t workspace_bytes,
+                        const tp_gemm_opts* opts, void* stream)
+{
+    return gemm_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, 1, splits, workspace, workspace_bytes, stream);
 }
 
 int tp_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -504,7 +637,10 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.m_tiles = static_cast<int>(pl.m_tiles);
     p.n_tiles = static_cast<int>(pl.n_tiles);
     p.k_blocks = static_cast<int>(pl.k_blocks);
+    p.splits = 1;
+    p.kb_per_split = p.k_blocks;
     p.group_m = group_m_for(opts, pl.m_tiles);
+    l2_hints_for(opts, &p.l2_a, &p.l2_b);
     p.conv_P = static_cast<int>(P);
     p.conv_Q = static_cast<int>(Q);
     p.conv_stride = static_cast<int>(stride);

@@ -95,7 +95,13 @@ struct GemmParams {
     int m_tiles;   // tiles of 128*CG rows
     int n_tiles;   // tiles of BN columns
     int k_blocks;  // 64-deep K blocks
+    // split-K: work unit u is tile u % tiles over K blocks
+    // [split * kb_per_split, min(k_blocks, (split + 1) * kb_per_split)),
+    // split = u / tiles; its fp32 partial goes to slice `split` of the
+    // workspace C map. splits == 1 is the plain GEMM.
+    int splits, kb_per_split;
     int group_m;   // tile raster: group_m M-tiles share a sweep over N
+    int l2_a, l2_b;  // L2 eviction priority of A / B loads (0 normal, 1 first, 2 last)
     // convolution only
     int conv_P, conv_Q, conv_stride, conv_pad, conv_S, conv_cblocks;
     // plain-load producer only (operands TMA cannot describe): A / B (or x /
@@ -122,6 +128,7 @@ struct KernelKey {
     int out_f32;
     int conv;
     int ldg;        // 1: plain-load producer instead of TMA
+    int splitk;     // 1: fp32 partials per K slice into a workspace
 };
 
 struct GemmLaunch {

@@ -158,7 +158,22 @@ __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA,
     }
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
+// Work unit u of a launch: output tile and its K-block range.
+struct Unit {
+    int tile, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& p)
+{
+    Unit w;
+    w.split = u / num_tiles;
+    w.tile = u - w.split * num_tiles;
+    w.kb0 = w.split * p.kb_per_split;
+    w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
+    return w;
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
 __global__ void __launch_bounds__(192, 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const GemmParams p)
@@ -166,6 +181,7 @@ __global__ void __launch_bounds__(192, 1)
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
     constexpr bool CL = (CG == 2);
     static_assert(!LDG || CG == 1, "the plain-load producer feeds the 1-SM atom");
+    static_assert(!SPLITK || (OUT_F32 && !CONV && !LDG), "split-K writes fp32 GEMM partials");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -218,6 +234,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_units = num_tiles * p.splits;
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
@@ -226,10 +243,11 @@ __global__ void __launch_bounds__(192, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+        for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+            const Unit w = unit_of(u, num_tiles, p);
             int mt, nt;
-            tile_coords(t, p, mt, nt);
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
+            tile_coords(w.tile, p, mt, nt);
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 int free_ok = 1;
                 if (lane == 0)
                     free_ok = wait_bounded<false>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
@@ -252,13 +270,16 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 0) {
         // --------------------------------------------------- producer ---
         if (elect_one()) {
+            const uint64_t pol_a = make_l2_policy(p.l2_a);
+            const uint64_t pol_b = make_l2_policy(p.l2_b);
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+            for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                const Unit w = unit_of(u, num_tiles, p);
                 int mt, nt;
-                tile_coords(t, p, mt, nt);
+                tile_coords(w.tile, p, mt, nt);
                 const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
                 const int n_row = nt * BN + static_cast<int>(rank) * Cfg::B_ROWS;
                 int img = 0, base_h = 0, base_w = 0;
@@ -271,7 +292,7 @@ __global__ void __launch_bounds__(192, 1)
                     base_h = pp * p.conv_stride - p.conv_pad;
                     base_w = qq * p.conv_stride - p.conv_pad;
                 }
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded<CL>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
@@ -287,20 +308,20 @@ __global__ void __launch_bounds__(192, 1)
                         const int sx = rs - r * p.conv_S;
                         if constexpr (CL) {
                             tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img,
-                                                    static_cast<uint16_t>(sx), static_cast<uint16_t>(r));
-                            tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row);
+                                                    static_cast<uint16_t>(sx), static_cast<uint16_t>(r), pol_a);
+                            tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row, pol_b);
                         } else {
                             tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img,
-                                               static_cast<uint16_t>(sx), static_cast<uint16_t>(r));
-                            tma_load_3d(dB, &mapB, fb, c0, rs, n_row);
+                                               static_cast<uint16_t>(sx), static_cast<uint16_t>(r), pol_a);
+                            tma_load_3d(dB, &mapB, fb, c0, rs, n_row, pol_b);
                         }
                     } else {
                         if constexpr (CL) {
-                            tma_load_2d_pair(dA, &mapA, fb, kb * Cfg::BK, m_row);
-                            tma_load_2d_pair(dB, &mapB, fb, kb * Cfg::BK, n_row);
+                            tma_load_2d_pair(dA, &mapA, fb, kb * Cfg::BK, m_row, pol_a);
+                            tma_load_2d_pair(dB, &mapB, fb, kb * Cfg::BK, n_row, pol_b);
                         } else {
-                            tma_load_2d(dA, &mapA, fb, kb * Cfg::BK, m_row);
-                            tma_load_2d(dB, &mapB, fb, kb * Cfg::BK, n_row);
+                            tma_load_2d(dA, &mapA, fb, kb * Cfg::BK, m_row, pol_a);
+                            tma_load_2d(dB, &mapB, fb, kb * Cfg::BK, n_row, pol_b);
                         }
                     }
                     ++issued;
@@ -337,13 +358,14 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t ph = 0;
                 int lt = 0;
                 bool ok = true;
-                for (int t = cluster_id; ok && t < num_tiles; t += num_clusters, ++lt) {
+                for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++lt) {
+                    const Unit w = unit_of(u, num_tiles, p);
                     const int b = lt & 1;
                     const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
                     if (!wait_bounded<CL>(acce_bar(b), aph ^ 1u, p.wait, abort_flag, SITE_MMA_ACC_EMPTY)) break;
                     tcgen05_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-                    for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!wait_bounded<CL>(full_bar(s), ph, p.wait, abort_flag, SITE_MMA_FULL)) {
                             ok = false;
                             break;
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(192, 1)
                         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                             const uint64_t da = umma_desc_sw128_kmajor(aS + k * 32);
                             const uint64_t db = umma_desc_sw128_kmajor(bS + k * 32);
-                            umma_bf16<CG>(d_tmem, da, db, IDESC, (kb | k) != 0 ? 1u : 0u);
+                            umma_bf16<CG>(d_tmem, da, db, IDESC, (kb != w.kb0 || k != 0) ? 1u : 0u);
                         }
                         if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
                         else umma_commit(empty_bar(s));
@@ -384,13 +406,14 @@ __global__ void __launch_bounds__(192, 1)
         constexpr int CHUNKS = BN / Cfg::EPI_COLS;
         int buf = 0;
         int lt = 0;
-        for (int t = cluster_id; t < num_tiles; t += num_clusters, ++lt) {
+        for (int u = cluster_id; u < num_units; u += num_clusters, ++lt) {
+            const Unit w = unit_of(u, num_tiles, p);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
             if (!wait_bounded<CL>(accf_bar(b), aph, p.wait, abort_flag, SITE_EPI_ACC_FULL)) break;
             tcgen05_fence_after();
             int mt, nt;
-            tile_coords(t, p, mt, nt);
+            tile_coords(w.tile, p, mt, nt);
             const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM + quarter * 32;
             const int n0 = nt * BN;
             int nchunks = 0;
@@ -452,7 +475,8 @@ __global__ void __launch_bounds__(192, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&mapC, sbuf, cs, m_row);
+                        if constexpr (SPLITK) tma_store_3d(&mapC, sbuf, cs, m_row, w.split);
+                        else tma_store_2d(&mapC, sbuf, cs, m_row);
                         bulk_commit_group();
                     }
                     buf ^= 1;
@@ -491,11 +515,11 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
 cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
-    auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG>;
+    auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -513,11 +537,11 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.params);
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
 constexpr KernelEntry mainloop_entry()
 {
-    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0},
-                       &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG>,
+    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0, SPLITK ? 1 : 0},
+                       &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>,
                        MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES};
 }
 

@@ -61,6 +61,22 @@ def skinny():
 
 @pytest.mark.parametrize("idx", [0, 1, 2])
 @pytest.mark.parametrize("out_f32", [True, False])
+def test_skinny_set_splitk(skinny, idx, out_f32):
+    (M, N, K), (A, B) = skinny[idx]
+    rows = {0: np.arange(1, 128, 2), 1: oracle.sample_rows(M, 32) + 1, 2: None}[idx]
+    if rows is not None:
+        rows = np.minimum(rows, M - 1)
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K, rows=rows)
+    ws = torch.empty(tp.tp_gemm_splitk_workspace_bytes(M, N, 16) // 4, dtype=torch.float32, device="cuda")
+    c = new_out(M, N, out_f32)
+    tp.tp_gemm_bf16_splitk(dev_bf16(A), dev_bf16(B), c, M, N, K, K, K, N, out_f32=out_f32, splits=0, workspace=ws)
+    expect_ok()
+    got = host_f64(c if rows is None else c.index_select(0, torch.from_numpy(rows).cuda()))
+    check_against_oracle(got, ref, ab, out_f32, f"skinny split-K {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2])
+@pytest.mark.parametrize("out_f32", [True, False])
 def test_skinny_set(skinny, idx, out_f32):
     (M, N, K), (A, B) = skinny[idx]
     rows = {0: np.arange(0, 128, 2), 1: oracle.sample_rows(M, 32), 2: None}[idx]

@@ -179,3 +179,13 @@ def test_plan_budget_errors():
     assert plan(256, 256, 256, atom=3)[0] == tp.TP_ERR_INVALID_ARG
     st, p = plan(256, 256, 256, atom=2, pipe_depth=8)
     assert st == tp.TP_OK and p["pipe_depth"] == 8
+
+
+def test_splitk_workspace_arithmetic():
+    assert tp.tp_gemm_splitk_workspace_bytes(128, 8192, 4) == 4 * 128 * 8192 * 4
+    assert tp.tp_gemm_splitk_workspace_bytes(300, 201, 3) == 3 * 300 * 204 * 4   # rows padded to 16 bytes
+    with pytest.raises(tp.TPError):
+        tp.tp_gemm_splitk_workspace_bytes(10, 10, 0)
+    ks = [k for k in tp.tp_list_kernels() if k["splitk"]]
+    assert {(k["atom"], k["tile_n"]) for k in ks} == {(1, 128), (1, 256), (2, 128), (2, 256)}
+    assert all(k["out_f32"] == 1 and k["conv"] == 0 for k in ks)
