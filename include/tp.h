@@ -45,7 +45,8 @@ typedef enum {
     TP_ERR_CUDA = 3,
     TP_ERR_DRIVER_ENCODE = 4,
     TP_ERR_TIMEOUT = 5,
-    TP_ERR_SMEM_BUDGET = 6
+    TP_ERR_SMEM_BUDGET = 6,
+    TP_ERR_WORKSPACE_LIMIT = 7
 } tp_status;
 
 /* Which code path a call took (tp_plan.path). */
@@ -137,6 +138,33 @@ TP_API int tp_gemm_bf16_splitk(const void* A, const void* B, void* C, int64_t M,
 /* Workspace bytes tp_gemm_bf16_splitk needs for `splits` slices:
  * splits x M x round_up(N, 4) x 4. Host-only. */
 TP_API int tp_gemm_splitk_workspace_bytes(int64_t M, int64_t N, int splits, int64_t* bytes);
+
+/*
+ * tp_gemm_bf16_splitk without a caller workspace, for callers that may not
+ * allocate device memory while they run (a fixed device-memory budget
+ * reserved up front by another allocator, or code where cudaMalloc's
+ * implicit device-wide synchronization is not allowed). The pages have no
+ * counterpart: this is a property of the library, not of the method.
+ *  - The partial sums live in a fixed 32 MiB array inside the library
+ *    (tp_gemm_splitk_noalloc_capacity()); every GPU that loads the library
+ *    holds it until the process exits. Nothing is allocated per call.
+ *  - The first call on a device looks up the array's device address for
+ *    that device; make that first call before any stream capture.
+ *  - An explicit `splits` whose workspace (tp_gemm_splitk_workspace_bytes)
+ *    exceeds the array returns TP_ERR_WORKSPACE_LIMIT; splits = 0 chooses
+ *    only counts that fit (one slice needs no workspace).
+ *  - Every call shares the one array and leaves its partials there. Each
+ *    call writes every partial it reads, so nothing has to start at zero,
+ *    but calls that overlap on the GPU (other streams, other threads) race
+ *    on it: serialize them.
+ * Arguments, layout and results are those of tp_gemm_bf16_splitk.
+ */
+TP_API int tp_gemm_bf16_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t ldb, int64_t ldc, int out_f32, int splits,
+                                       void* stream);
+
+/* Bytes of the fixed workspace array behind tp_gemm_bf16_splitk_noalloc. */
+TP_API int64_t tp_gemm_splitk_noalloc_capacity(void);
 
 /*
  * Forward convolution as an implicit GEMM on the same mainloop; the A tile is

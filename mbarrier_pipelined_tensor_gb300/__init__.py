@@ -31,6 +31,7 @@ TP_ERR_CUDA = 3
 TP_ERR_DRIVER_ENCODE = 4
 TP_ERR_TIMEOUT = 5
 TP_ERR_SMEM_BUDGET = 6
+TP_ERR_WORKSPACE_LIMIT = 7
 
 TP_PATH_NONE = 0
 TP_PATH_MAINLOOP = 1
@@ -77,6 +78,8 @@ _SIGS = {
     "tp_gemm_bf16_ex": ([_P, _P, _P] + [_I64] * 6 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_gemm_bf16_splitk": ([_P, _P, _P] + [_I64] * 6 + [_I, _I, _P, _I64, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_gemm_splitk_workspace_bytes": ([_I64, _I64, _I, ctypes.POINTER(_I64)], _I),
+    "tp_gemm_bf16_splitk_noalloc": ([_P, _P, _P] + [_I64] * 6 + [_I, _I, _P], _I),
+    "tp_gemm_splitk_noalloc_capacity": ([], _I64),
     "tp_conv2d_fprop_bf16": ([_P, _P, _P] + [_I64] * 9 + [_P], _I),
     "tp_conv2d_fprop_bf16_ex": ([_P, _P, _P] + [_I64] * 9 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_tma_copy_2d": ([_P, _P, _I64, _I64, _I64, _P], _I),
@@ -174,6 +177,17 @@ def tp_gemm_splitk_workspace_bytes(M, N, splits) -> int:
     b = _I64()
     _check(_lib.tp_gemm_splitk_workspace_bytes(M, N, splits, ctypes.byref(b)), "tp_gemm_splitk_workspace_bytes")
     return int(b.value)
+
+
+def tp_gemm_bf16_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, splits=0, stream=None):
+    """Split-K GEMM whose workspace is the library's fixed array (no allocation)."""
+    _check(_lib.tp_gemm_bf16_splitk_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc,
+                                            int(bool(out_f32)), splits, _stream(stream)),
+           "tp_gemm_bf16_splitk_noalloc")
+
+
+def tp_gemm_splitk_noalloc_capacity() -> int:
+    return int(_lib.tp_gemm_splitk_noalloc_capacity())
 
 
 def tp_conv2d_fprop_bf16(x, w, y, N, H, W, C, K, R, S, stride, pad, stream=None):

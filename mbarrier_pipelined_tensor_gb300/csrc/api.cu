@@ -334,6 +334,7 @@ const char* tp_status_string(int s)
     case TP_ERR_DRIVER_ENCODE: return "TP_ERR_DRIVER_ENCODE";
     case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
     case TP_ERR_SMEM_BUDGET: return "TP_ERR_SMEM_BUDGET";
+    case TP_ERR_WORKSPACE_LIMIT: return "TP_ERR_WORKSPACE_LIMIT";
     default: return "TP_ERR_UNKNOWN";
     }
 }
@@ -782,5 +783,70 @@ int tp_selftest_wait_timeout(uint32_t limit_us, void* stream)
     cudaError_t e = launch_wait_selftest(w, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
+
+// ------------------------------------------- split-K without allocation ---
+//
+// Some callers may not allocate device memory while they run: code that lives
+// inside a fixed device-memory budget reserved up front by another allocator,
+// or code where cudaMalloc's implicit device-wide synchronization is not
+// allowed. tp_gemm_bf16_splitk_noalloc serves them with a workspace that is a
+// fixed array inside the library instead of a caller buffer.
+
+}  // extern "C"
+
+namespace {
+
+constexpr int64_t kNoallocWorkspaceBytes = 32ll << 20;  // 32 MiB per GPU
+
+// The split-K partial sums of tp_gemm_bf16_splitk_noalloc. Every GPU that
+// loads the library holds this array until the process exits. In host code
+// the name is only a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_workspace[kNoallocWorkspaceBytes / sizeof(float)];
+
+float* g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: the array's device address.
+int noalloc_workspace(float** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return TP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return TP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tp_gemm_bf16_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldc, int out_f32, int splits, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0 || splits < 0) return TP_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TP_OK;
+    if (splits > 0 && K > 0) {
+        int sp = splits, kps = 0;
+        normalize_splits(cdiv(K, 64), &sp, &kps);
+        if (sp > 1 && static_cast<int64_t>(sp) * M * splitk_ldw(N) * 4 > kNoallocWorkspaceBytes)
+            return TP_ERR_WORKSPACE_LIMIT;
+    }
+    float* ws = nullptr;
+    const int st = noalloc_workspace(&ws);
+    if (st) return st;
+    return gemm_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, nullptr, 1, splits, ws, kNoallocWorkspaceBytes,
+                     stream);
+}
+
+int64_t tp_gemm_splitk_noalloc_capacity(void) { return kNoallocWorkspaceBytes; }
 
 }  // extern "C"

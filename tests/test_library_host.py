@@ -19,7 +19,7 @@ AL = 1 << 20  # a 16-byte aligned fake device address (nothing is launched)
 
 def header_functions():
     text = open(HEADER).read()
-    return re.findall(r"^TP_API\s+(?:const\s+char\s*\*|int)\s+(tp_\w+)\(", text, flags=re.M)
+    return re.findall(r"^TP_API\s+(?:const\s+char\s*\*|int64_t|int)\s+(tp_\w+)\(", text, flags=re.M)
 
 
 def test_every_declared_symbol_is_exported():
