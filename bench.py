@@ -313,7 +313,26 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
     gbs = moved / (ms * 1e-3) / 1e9
     rows["tma_copy_1GiB"] = {"unit": "GB/s", "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3),
                              "ms": round(ms, 4), "bit_exact": bool(torch.equal(src, dst))}
+    del dst
+    # 1 GiB TMA transpose of the same matrix (dst 16384 x 32768)
+    dst = torch.empty((cc, rr), dtype=torch.int16, device="cuda")
+    tr = lambda: tp.tp_tma_transpose_2d(src, dst, rr, cc, cc, rr, stream=s)  # noqa: E731
+    for _ in range(3):
+        tr()
+    ms = time_loop(torch, stream, tr, n) / n
+    gbs = moved / (ms * 1e-3) / 1e9
+    rows["tma_transpose_1GiB"] = {"unit": "GB/s", "gbs": round(gbs, 1),
+                                  "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3), "ms": round(ms, 4),
+                                  "bit_exact": bool(torch.equal(dst, src.t()))}
     del src, dst
+
+    # dependent fma chains (RAW latency upper bound, SM cycles per link)
+    probe = {}
+    for kind, name in ((0, "ffma_f32"), (1, "dfma_f64")):
+        res, cpl = tp.tp_probe_fma_latency(kind, 64 * 4096, 3.0, stream=s)
+        probe[name] = {"cycles_per_link": round(cpl, 3), "exact": res == 3.0 + 64 * 4096}
+    probe["pages_b200"] = {"ffma_f32": 4, "dfma_f64": 8}
+    rows["fma_chain_latency"] = probe
     return rows
 
 

@@ -56,7 +56,9 @@ enum {
     TP_PATH_ZERO_FILL = 2,     /* K == 0: C is the empty sum */
     TP_PATH_TMA_COPY = 3,      /* TMA load -> smem -> TMA store ring */
     TP_PATH_VEC_COPY = 4,      /* vectorized ld/st fallback copy */
-    TP_PATH_FALLBACK_MAINLOOP = 5  /* plain-load producer + tcgen05 mainloop */
+    TP_PATH_FALLBACK_MAINLOOP = 5, /* plain-load producer + tcgen05 mainloop */
+    TP_PATH_TMA_TRANSPOSE = 6,     /* TMA load -> ldmatrix/stmatrix.trans -> TMA store */
+    TP_PATH_VEC_TRANSPOSE = 7      /* shared-memory tile transpose fallback */
 };
 
 /*
@@ -211,6 +213,28 @@ typedef struct {
 TP_API int tp_tma_copy_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld,
                       const tp_copy_opts* opts, void* stream);
 
+/*
+ * dst = transpose(src), bit for bit, for 2-byte elements: src is rows x cols
+ * with row pitch ld_src (>= cols), dst is cols x rows with row pitch ld_dst
+ * (>= rows): dst[c*ld_dst + r] = src[r*ld_src + c]. The copy ring of "B200
+ * Tma Pipeline Designer" (steps 4-7) with a transpose between load and
+ * store: 64x64 tiles arrive by TMA with 128-byte swizzle, each warp turns
+ * them around in shared memory (ldmatrix / stmatrix.trans) and a TMA store
+ * writes them at the swapped coordinates, drained with commit_group /
+ * wait_group. Buffers TMA cannot describe (base not 16-byte aligned, a pitch
+ * times 2 not a multiple of 16), copies under 64 KiB, and destination columns
+ * past the last multiple of 8 take a 32x32 shared-memory tile transpose.
+ * src and dst must not overlap; both must be 2-byte aligned.
+ */
+TP_API int tp_tma_transpose_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src,
+                               int64_t ld_dst, void* stream);
+
+/* The transpose with ring choices: opts->stages in {2,4,6,8}, ctas_per_sm
+ * (persistent one-warp CTAs per SM), force_vec; box fields are ignored (the
+ * tile is 64x64). */
+TP_API int tp_tma_transpose_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src,
+                                  int64_t ld_dst, const tp_copy_opts* opts, void* stream);
+
 /* Synchronizes `stream`, returns the current device's status (TP_OK or the
  * first device-side failure since the last call, e.g. TP_ERR_TIMEOUT from a
  * bounded barrier wait) and clears it. Returns TP_ERR_CUDA when the
@@ -274,6 +298,19 @@ typedef struct {
 /* Writes up to cap compiled variants to out (may be NULL) and returns how
  * many there are. Host-only. */
 TP_API int tp_list_kernels(tp_kernel_desc* out, int cap);
+
+/*
+ * Read-after-write latency of a fused multiply-add, measured on this GPU
+ * ("hardware-hazards-b200" note, "Fixed-latency RAW under-stalls": a chain
+ * a = a*1 + 1 whose result must be exactly seed + chain). One thread runs
+ * `chain` dependent fma.rn links (kind 0: fp32, kind 1: fp64; chain a
+ * multiple of 64, at most 2^26) between two clock64 reads. Writes the chain's
+ * result and the SM cycles per link, an upper bound on the latency (loop and
+ * clock-read overhead included). Synchronizes `stream`. The note's B200
+ * figures: 4 cycles fp32, 8 cycles fp64.
+ */
+TP_API int tp_probe_fma_latency(int kind, int chain, double seed, double* result, double* cycles_per_link,
+                                void* stream);
 
 /* Launches one CTA that waits on an mbarrier nothing arrives on, with a
  * limit of limit_us microseconds: the wait must give up and record

@@ -39,6 +39,8 @@ TP_PATH_ZERO_FILL = 2
 TP_PATH_TMA_COPY = 3
 TP_PATH_VEC_COPY = 4
 TP_PATH_FALLBACK_MAINLOOP = 5
+TP_PATH_TMA_TRANSPOSE = 6
+TP_PATH_VEC_TRANSPOSE = 7
 
 
 class tp_gemm_opts(ctypes.Structure):
@@ -84,6 +86,8 @@ _SIGS = {
     "tp_conv2d_fprop_bf16_ex": ([_P, _P, _P] + [_I64] * 9 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_tma_copy_2d": ([_P, _P, _I64, _I64, _I64, _P], _I),
     "tp_tma_copy_2d_ex": ([_P, _P, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
+    "tp_tma_transpose_2d": ([_P, _P, _I64, _I64, _I64, _I64, _P], _I),
+    "tp_tma_transpose_2d_ex": ([_P, _P, _I64, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
     "tp_device_status": ([_P], _I),
     "tp_device_status_detail": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "tp_status_string": ([_I], ctypes.c_char_p),
@@ -94,6 +98,8 @@ _SIGS = {
     "tp_last_plan": ([ctypes.POINTER(tp_plan)], _I),
     "tp_list_kernels": ([ctypes.POINTER(tp_kernel_desc), _I], _I),
     "tp_selftest_wait_timeout": ([ctypes.c_uint32, _P], _I),
+    "tp_probe_fma_latency": ([_I, _I, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
+                              ctypes.POINTER(ctypes.c_double), _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -213,6 +219,18 @@ def tp_tma_copy_2d_ex(src, dst, rows, cols, ld, stream=None, box_cols=0, box_row
            "tp_tma_copy_2d_ex")
 
 
+def tp_tma_transpose_2d(src, dst, rows, cols, ld_src, ld_dst, stream=None):
+    _check(_lib.tp_tma_transpose_2d(_ptr(src), _ptr(dst), rows, cols, ld_src, ld_dst, _stream(stream)),
+           "tp_tma_transpose_2d")
+
+
+def tp_tma_transpose_2d_ex(src, dst, rows, cols, ld_src, ld_dst, stream=None, stages=0, ctas_per_sm=0,
+                           force_vec=False):
+    o = tp_copy_opts(0, 0, stages, ctas_per_sm, int(bool(force_vec)))
+    _check(_lib.tp_tma_transpose_2d_ex(_ptr(src), _ptr(dst), rows, cols, ld_src, ld_dst, ctypes.byref(o),
+                                       _stream(stream)), "tp_tma_transpose_2d_ex")
+
+
 def tp_device_status(stream=None) -> int:
     """Synchronizes the stream; returns (and clears) the device status code."""
     return int(_lib.tp_device_status(_stream(stream)))
@@ -252,6 +270,14 @@ def tp_list_kernels():
     arr = (tp_kernel_desc * n)()
     _lib.tp_list_kernels(arr, n)
     return [{f: getattr(a, f) for f, _ in tp_kernel_desc._fields_} for a in arr]
+
+
+def tp_probe_fma_latency(kind: int, chain: int = 65536, seed: float = 0.0, stream=None):
+    """Returns (chain result, SM cycles per dependent fma link); kind 0 fp32, 1 fp64."""
+    r, c = ctypes.c_double(), ctypes.c_double()
+    _check(_lib.tp_probe_fma_latency(kind, chain, seed, ctypes.byref(r), ctypes.byref(c), _stream(stream)),
+           "tp_probe_fma_latency")
+    return r.value, c.value
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None):

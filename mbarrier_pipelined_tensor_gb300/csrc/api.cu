@@ -29,6 +29,12 @@ cudaError_t launch_vec_copy(const void* src, void* dst, int64_t rows, int64_t co
                             cudaStream_t st);
 cudaError_t launch_zero_fill(void* c, int64_t M, int64_t N, int64_t ldc, int elem_bytes, cudaStream_t st);
 cudaError_t launch_wait_selftest(const WaitCtl& w, cudaStream_t st);
+int transpose_smem_bytes(int stages);
+cudaError_t run_fma_probe(int kind, double seed, int blocks, cudaStream_t st, double* result, long long* cycles);
+cudaError_t launch_tma_transpose(int stages, const CUtensorMap& s, const CUtensorMap& d, int tiles_x, int tiles_y,
+                                 const WaitCtl& w, int grid, cudaStream_t st);
+cudaError_t launch_vec_transpose(const void* src, void* dst, int64_t r0, int64_t rows, int64_t cols, int64_t ld_src,
+                                 int64_t ld_dst, int sm_count, cudaStream_t st);
 }  // namespace tp
 
 using namespace tp;
@@ -95,6 +101,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// fp32 workspace row of split-K: N rounded up to whole 16-byte granules.
+int64_t splitk_ldw(int64_t N) { return (N + 3) / 4 * 4; }
+
 // ------------------------------------------------------ variant table ---
 
 constexpr int kTables = 5;
@@ -153,7 +162,7 @@ int deepest_fitting(int atom, int tile_n)
 // measured throughput on a large square GEMM relative to the best one
 // (2-SM, N = 256 at its deepest ring). A fixed field (*atom or *tile_n
 // nonzero) restricts the candidates.
-void choose_variant(int64_t M, int64_t N, int sm_count, int* atom, int* tile_n)
+void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* atom, int* tile_n)
 {
     struct Cand {
         int atom, tile_n;
@@ -167,7 +176,11 @@ void choose_variant(int64_t M, int64_t N, int sm_count, int* atom, int* tile_n)
         if ((*atom && c.atom != *atom) || (*tile_n && c.tile_n != *tile_n)) continue;
         const int64_t tiles = cdiv(M, 128 * c.atom) * cdiv(N, c.tile_n);
         const int64_t clusters = std::max<int64_t>(1, sm_count / c.atom);
-        const double cost = static_cast<double>(cdiv(tiles, clusters)) * c.tile_n / c.eff;
+        double cost = static_cast<double>(cdiv(tiles, clusters)) * c.tile_n / c.eff;
+        // Short K: a narrow tile's fixed per-tile cost (ring fill, epilogue)
+        // is a larger share of its work (4096 x 4096 x 512: N = 128 tiles
+        // measured 27 us against 23 us for N = 256).
+        if (k_blocks <= 16 && c.tile_n == 128) cost *= 1.25;
         if (!have || cost < best) {
             best = cost;
             pick = c;
@@ -192,7 +205,7 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
         atom = 1;
         tile_n = 128;
     }
-    if (atom == 0 || tile_n == 0) choose_variant(M, N, sm_count, &atom, &tile_n);
+    if (atom == 0 || tile_n == 0) choose_variant(M, N, k_blocks, sm_count, &atom, &tile_n);
     int depth = o && o->pipe_depth ? o->pipe_depth : deepest_fitting(atom, tile_n);
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
     const int64_t smem = mainloop_smem(atom, depth, tile_n);
@@ -225,23 +238,19 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     return TP_OK;
 }
 
-// K slices for split-K: the count with the least estimated time,
-// waves x K blocks per slice, plus the partial-sum traffic (each extra slice
-// writes and re-reads one fp32 tile, about two K blocks of operand loads).
-int choose_splits(int64_t tiles, int64_t clusters, int64_t k_blocks)
+// K slices for split-K. Splitting pays only when the output tiles leave most
+// of the GPU idle and the fp32 partials (written and re-read once per slice)
+// stay small next to the operands: on a GB300, 128 x 8192 x 16384 gains 12%
+// with 2 slices, while 4096 x 4096 x 512 loses 3x and 1000^3 loses 25%.
+int choose_splits(int64_t tiles, int64_t clusters, int64_t k_blocks, int64_t M, int64_t N, int64_t K)
 {
-    int best_s = 1;
-    double best = 0;
-    for (int s = 1; s <= 16 && s <= k_blocks; ++s) {
-        const int64_t units = tiles * s;
-        const double cost = static_cast<double>(cdiv(units, clusters)) * static_cast<double>(cdiv(k_blocks, s)) +
-                            (s > 1 ? 2.0 * s * static_cast<double>(tiles) / static_cast<double>(clusters) : 0.0);
-        if (s == 1 || cost < best) {
-            best = cost;
-            best_s = s;
-        }
-    }
-    return best_s;
+    if (tiles * 2 > clusters) return 1;
+    int64_t s = clusters / tiles;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, k_blocks / 4));
+    s = std::min<int64_t>(s, 16);
+    const double operand_bytes = 2.0 * static_cast<double>(M * K + N * K);
+    while (s > 1 && 8.0 * static_cast<double>(s * M * splitk_ldw(N)) > 0.25 * operand_bytes) --s;
+    return static_cast<int>(s);
 }
 
 // Slices actually used so that none is empty.
@@ -254,7 +263,7 @@ void normalize_splits(int64_t k_blocks, int* splits, int* kb_per_split)
     *splits = static_cast<int>(cdiv(k_blocks, kps));
 }
 
-int64_t splitk_ldw(int64_t N) { return (N + 3) / 4 * 4; }
+
 
 int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
 {
@@ -405,6 +414,14 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     DeviceState* dev = nullptr;
     int st = device_state(&dev);
     if (st) return st;
+    // Split-K of a single-tile-row problem (M <= 128): the 2-SM atom would
+    // compute a pair tile half of which is out of bounds; use the 1-SM atom.
+    tp_gemm_opts local{};
+    if (splitk && M <= 128 && !(opts && opts->atom)) {
+        if (opts) local = *opts;
+        local.atom = 1;
+        opts = &local;
+    }
     st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, dev->sm_count, &pl);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -424,7 +441,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
         const int64_t tiles = pl.m_tiles * pl.n_tiles;
         const int64_t clusters = std::max<int64_t>(1, (opts && opts->max_ctas > 0 ? opts->max_ctas : dev->sm_count) /
                                                           pl.atom);
-        int sp = splits > 0 ? splits : choose_splits(tiles, clusters, pl.k_blocks);
+        int sp = splits > 0 ? splits : choose_splits(tiles, clusters, pl.k_blocks, M, N, K);
         if (splits == 0 && sp > cap) sp = static_cast<int>(std::max<int64_t>(1, cap));
         normalize_splits(pl.k_blocks, &sp, &kps);
         if (sp > 1) {
@@ -750,6 +767,77 @@ int tp_tma_copy_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64
     return tp_tma_copy_2d_ex(src, dst, rows, cols, ld, nullptr, stream);
 }
 
+int tp_tma_transpose_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst,
+                           const tp_copy_opts* o, void* stream)
+{
+    tp_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    t_last_plan = pl;
+    if (rows < 0 || cols < 0 || ld_src < cols || ld_dst < rows) return TP_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return TP_OK;
+    if (!src || !dst) return TP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 1u) return TP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int stages = o && o->stages ? o->stages : 4;
+    const int per_sm = o && o->ctas_per_sm ? o->ctas_per_sm : 4;
+    if (stages != 2 && stages != 4 && stages != 6 && stages != 8) return TP_ERR_INVALID_ARG;
+    if (per_sm < 1) return TP_ERR_INVALID_ARG;
+    // TMA stores write whole 16-byte granules of a destination row: the TMA
+    // path covers destination columns (source rows) 0..rows_tma-1, the rest
+    // goes through the shared-memory tile transpose.
+    const int64_t rows_tma = rows / 8 * 8;
+    const bool tma_ok = aligned16(src) && aligned16(dst) && (ld_src * 2) % 16 == 0 && (ld_dst * 2) % 16 == 0 &&
+                        rows * cols * 2 >= 65536 && rows_tma > 0 && rows <= INT32_MAX && cols <= INT32_MAX &&
+                        !(o && o->force_vec);
+    if (!tma_ok) {
+        cudaError_t e = launch_vec_transpose(src, dst, 0, rows, cols, ld_src, ld_dst, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        pl.path = TP_PATH_VEC_TRANSPOSE;
+        t_last_plan = pl;
+        return TP_OK;
+    }
+    const int smem = transpose_smem_bytes(stages);
+    if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
+    TiledDesc ds{CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(src),
+                 {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)}, {static_cast<uint64_t>(ld_src) * 2},
+                 {64, 64}, CU_TENSOR_MAP_SWIZZLE_128B};
+    TiledDesc dd{CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, dst,
+                 {static_cast<uint64_t>(rows_tma), static_cast<uint64_t>(cols)}, {static_cast<uint64_t>(ld_dst) * 2},
+                 {64, 64}, CU_TENSOR_MAP_SWIZZLE_128B};
+    CUtensorMap ms, md;
+    if ((st = encode_tiled(&ms, ds)) || (st = encode_tiled(&md, dd))) return st;
+    const int64_t tiles_x = cdiv(cols, 64), tiles_y = cdiv(rows_tma, 64);
+    if (tiles_x * tiles_y > INT32_MAX) return TP_ERR_UNSUPPORTED;
+    int64_t grid = static_cast<int64_t>(dev->sm_count) * per_sm;
+    if (grid > tiles_x * tiles_y) grid = tiles_x * tiles_y;
+    cudaError_t e = launch_tma_transpose(stages, ms, md, static_cast<int>(tiles_x), static_cast<int>(tiles_y),
+                                         WaitCtl{dev->status, wait_limit_ns()}, static_cast<int>(grid), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (rows_tma < rows) {
+        e = launch_vec_transpose(src, dst, rows_tma, rows - rows_tma, cols, ld_src, ld_dst, dev->sm_count, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    pl.path = TP_PATH_TMA_TRANSPOSE;
+    pl.pipe_depth = stages;
+    pl.grid = static_cast<int>(grid);
+    pl.cluster = 1;
+    pl.smem_bytes = smem;
+    pl.m_tiles = tiles_y;
+    pl.n_tiles = tiles_x;
+    pl.splits = 1;
+    t_last_plan = pl;
+    return TP_OK;
+}
+
+int tp_tma_transpose_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst,
+                        void* stream)
+{
+    return tp_tma_transpose_2d_ex(src, dst, rows, cols, ld_src, ld_dst, nullptr, stream);
+}
+
 int tp_device_status_detail(void* stream, int* site, int* block, int* thread)
 {
     DeviceState* dev = nullptr;
@@ -772,6 +860,20 @@ int tp_device_status_detail(void* stream, int* site, int* block, int* thread)
 }
 
 int tp_device_status(void* stream) { return tp_device_status_detail(stream, nullptr, nullptr, nullptr); }
+
+int tp_probe_fma_latency(int kind, int chain, double seed, double* result, double* cycles_per_link, void* stream)
+{
+    if ((kind != 0 && kind != 1) || chain < 64 || chain % 64 || chain > (1 << 26) || !result || !cycles_per_link)
+        return TP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    long long cycles = 0;
+    cudaError_t e = run_fma_probe(kind, seed, chain / 64, static_cast<cudaStream_t>(stream), result, &cycles);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *cycles_per_link = static_cast<double>(cycles) / static_cast<double>(chain);
+    return TP_OK;
+}
 
 int tp_selftest_wait_timeout(uint32_t limit_us, void* stream)
 {

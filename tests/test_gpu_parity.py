@@ -303,3 +303,18 @@ def test_conv_centre_delta_bit_exact():
     tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, C, 3, 3, 1, 1, out_f32=True, atom=1)
     expect_ok()
     assert np.array_equal(host_f64(y), datagen.bf16_to_f32(x).astype(np.float64).reshape(-1, C))
+
+
+# ------------------------------------------------------- latency probe ---
+
+@pytest.mark.parametrize("kind,floor,ceiling", [(0, 4, 16), (1, 8, 512)])
+def test_fma_chain_latency_probe(kind, floor, ceiling):
+    # The chain's result is exact (seed + chain < 2^24); the cycles per link
+    # bound the RAW latency from above. The hazards note measured 4 (fp32)
+    # and 8 (fp64) cycles on B200; GB300's fp64 path is far slower (about 64
+    # cycles per dependent DFMA), so only plausibility is checked.
+    seed, chain = 3.0, 64 * 1024
+    result, cpl = tp.tp_probe_fma_latency(kind, chain, seed)
+    assert result == seed + chain
+    assert 1.0 <= cpl <= ceiling
+    print(f"kind {kind}: {cpl:.2f} cycles per dependent fma (B200 note: {floor})")
