@@ -95,6 +95,9 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
  *               1 none, 2 A evict-last / B evict-first, 3 A evict-last,
  *               4 B evict-first.
+ *   no_tail:    1 keeps whole tiles in the last wave (the 2-SM, N = 256
+ *               variant otherwise runs a partial last wave as half-width
+ *               tiles).
  * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
  * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
  * "StageCount<9> fails the capacity assert"; a combination that fits but is
@@ -107,6 +110,7 @@ typedef struct {
     int group_m;
     int max_ctas;
     int l2_hint;
+    int no_tail;
 } tp_gemm_opts;
 
 /* tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit choices (opts may be NULL).
@@ -274,6 +278,7 @@ typedef struct {
     int smem_bytes;  /* dynamic shared memory per CTA */
     int64_t m_tiles, n_tiles, k_blocks;
     int splits;      /* K slices (1 unless split-K ran) */
+    int tail_units;  /* half-width units of the last wave (0: none) */
 } tp_plan;
 
 /*

@@ -45,7 +45,8 @@ TP_PATH_VEC_TRANSPOSE = 7
 
 class tp_gemm_opts(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int), ("l2_hint", ctypes.c_int)]
+                ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int), ("l2_hint", ctypes.c_int),
+                ("no_tail", ctypes.c_int)]
 
 
 class tp_copy_opts(ctypes.Structure):
@@ -58,7 +59,7 @@ class tp_plan(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("out_f32", ctypes.c_int), ("conv", ctypes.c_int),
                 ("grid", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
-                ("splits", ctypes.c_int)]
+                ("splits", ctypes.c_int), ("tail_units", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -159,8 +160,8 @@ def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
            "tp_gemm_bf16_f32")
 
 
-def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0):
-    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint)
+def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_tail=0):
+    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint, int(bool(no_tail)))
 
 
 def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):

@@ -176,7 +176,12 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
         if ((*atom && c.atom != *atom) || (*tile_n && c.tile_n != *tile_n)) continue;
         const int64_t tiles = cdiv(M, 128 * c.atom) * cdiv(N, c.tile_n);
         const int64_t clusters = std::max<int64_t>(1, sm_count / c.atom);
-        double cost = static_cast<double>(cdiv(tiles, clusters)) * c.tile_n / c.eff;
+        double waves = static_cast<double>(cdiv(tiles, clusters));
+        // The 2-SM, N = 256 variant runs a partial last wave that fits twice
+        // as half-width units: after at least one full wave it counts half.
+        const int64_t r = tiles % clusters;
+        if (c.atom == 2 && c.tile_n == 256 && tiles >= clusters && r > 0 && 2 * r <= clusters) waves -= 0.5;
+        double cost = waves * c.tile_n / c.eff;
         // Short K: a narrow tile's fixed per-tile cost (ring fill, epilogue)
         // is a larger share of its work (4096 x 4096 x 512: N = 128 tiles
         // measured 27 us against 23 us for N = 256).
@@ -264,6 +269,32 @@ void normalize_splits(int64_t k_blocks, int* splits, int* kb_per_split)
 }
 
 
+
+// Narrow tail for the 2-SM atom at N = 256: when the tiles left for the last,
+// partial wave (r = tiles mod clusters) fit twice into one wave, they run as
+// 2r half-width units, so that wave takes about half as long. A problem with
+// fewer tiles than clusters is all tail: its tiles run as half-width units on
+// twice as many clusters.
+void set_narrow_tail(tp_plan& pl, GemmParams& p, int64_t max_clusters)
+{
+    p.n_full = 0;
+    p.tail_units = 0;
+    if (pl.atom != 2 || pl.tile_n != 256 || max_clusters < 2) return;
+    const int64_t tiles = pl.m_tiles * pl.n_tiles;
+    const int64_t r = tiles % max_clusters;
+    if (r == 0 || 2 * r > max_clusters) return;
+    p.n_full = static_cast<int>(tiles - r);
+    p.tail_units = static_cast<int>(2 * r);
+    const int64_t clusters = tiles >= max_clusters ? max_clusters : 2 * r;
+    pl.grid = static_cast<int>(clusters * pl.atom);
+    pl.tail_units = p.tail_units;
+}
+
+int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom)
+{
+    const int64_t c = (o && o->max_ctas > 0) ? o->max_ctas / atom : sm_count / atom;
+    return c < 1 ? 1 : c;
+}
 
 int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
 {
@@ -391,7 +422,12 @@ int tp_gemm_plan(const void* A, const void* B, const void* C, int64_t M, int64_t
         if (st) return st;
         sm_count = d->sm_count;
     }
-    return gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32 ? 1 : 0, opts, sm_count, plan);
+    const int st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32 ? 1 : 0, opts, sm_count, plan);
+    if (st == TP_OK && plan->path == TP_PATH_MAINLOOP && !(opts && opts->no_tail)) {
+        GemmParams unused{};
+        set_narrow_tail(*plan, unused, max_clusters_for(opts, sm_count, plan->atom));
+    }
+    return st;
 }
 
 }  // extern "C"
@@ -500,6 +536,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.k_blocks = static_cast<int>(pl.k_blocks);
     p.splits = use_splitk ? pl.splits : 1;
     p.kb_per_split = use_splitk ? kps : p.k_blocks;
+    if (!use_splitk && !(opts && opts->no_tail))
+        set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
     p.group_m = group_m_for(opts, pl.m_tiles);
     l2_hints_for(opts, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
@@ -657,6 +695,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.k_blocks = static_cast<int>(pl.k_blocks);
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
+    if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
     p.group_m = group_m_for(opts, pl.m_tiles);
     l2_hints_for(opts, &p.l2_a, &p.l2_b);
     p.conv_P = static_cast<int>(P);

@@ -100,6 +100,10 @@ struct GemmParams {
     // split = u / tiles; its fp32 partial goes to slice `split` of the
     // workspace C map. splits == 1 is the plain GEMM.
     int splits, kb_per_split;
+    // Narrow tail (2-SM atom, splits == 1): units [0, n_full) are whole
+    // tiles; the last tail_units units are half-width tiles (N = BN/2), two
+    // per remaining tile, so the last, partial wave takes about half as long.
+    int n_full, tail_units;
     int group_m;   // tile raster: group_m M-tiles share a sweep over N
     int l2_a, l2_b;  // L2 eviction priority of A / B loads (0 normal, 1 first, 2 last)
     // convolution only

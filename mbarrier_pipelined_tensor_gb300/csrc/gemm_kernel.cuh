@@ -158,18 +158,29 @@ __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA,
     }
 }
 
-// Work unit u of a launch: output tile and its K-block range.
+// Work unit u of a launch: output tile, its K-block range, and which half
+// of the tile's columns it covers (-1: the whole tile).
 struct Unit {
-    int tile, split, kb0, kb1;
+    int tile, split, kb0, kb1, half;
 };
 
 __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& p)
 {
     Unit w;
+    if (p.tail_units > 0 && u >= p.n_full) {
+        const int v = u - p.n_full;
+        w.tile = p.n_full + (v >> 1);
+        w.half = v & 1;
+        w.split = 0;
+        w.kb0 = 0;
+        w.kb1 = p.k_blocks;
+        return w;
+    }
     w.split = u / num_tiles;
     w.tile = u - w.split * num_tiles;
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
+    w.half = -1;
     return w;
 }
 
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int num_tiles = p.m_tiles * p.n_tiles;
-    const int num_units = num_tiles * p.splits;
+    const int num_units = p.tail_units > 0 ? p.n_full + p.tail_units : num_tiles * p.splits;
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
@@ -281,7 +292,10 @@ __global__ void __launch_bounds__(192, 1)
                 int mt, nt;
                 tile_coords(w.tile, p, mt, nt);
                 const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
-                const int n_row = nt * BN + static_cast<int>(rank) * Cfg::B_ROWS;
+                // A half-width unit (2-SM only) needs BN/4 rows of B per CTA,
+                // starting at its half; the B box (BN/2 rows) loads them first.
+                const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
+                                             : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
                 int img = 0, base_h = 0, base_w = 0;
                 if constexpr (CONV) {
                     const int pq = p.conv_P * p.conv_Q;
@@ -354,6 +368,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!CL || leader) {
             if (elect_one()) {
                 constexpr uint32_t IDESC = umma_idesc_bf16_f32(Cfg::BM * CG, BN);
+                constexpr uint32_t IDESC_HALF = umma_idesc_bf16_f32(Cfg::BM * CG, BN / 2);
                 int s = 0;
                 uint32_t ph = 0;
                 int lt = 0;
@@ -377,7 +392,8 @@ __global__ void __launch_bounds__(192, 1)
                         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                             const uint64_t da = umma_desc_sw128_kmajor(aS + k * 32);
                             const uint64_t db = umma_desc_sw128_kmajor(bS + k * 32);
-                            umma_bf16<CG>(d_tmem, da, db, IDESC, (kb != w.kb0 || k != 0) ? 1u : 0u);
+                            umma_bf16<CG>(d_tmem, da, db, w.half < 0 ? IDESC : IDESC_HALF,
+                                          (kb != w.kb0 || k != 0) ? 1u : 0u);
                         }
                         if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
                         else umma_commit(empty_bar(s));
@@ -415,11 +431,12 @@ __global__ void __launch_bounds__(192, 1)
             int mt, nt;
             tile_coords(w.tile, p, mt, nt);
             const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM + quarter * 32;
-            const int n0 = nt * BN;
+            const int n0 = nt * BN + (w.half < 0 ? 0 : w.half * (BN / 2));
+            const int max_chunks = w.half < 0 ? CHUNKS : CHUNKS / 2;
             int nchunks = 0;
-            if (m_row < p.M) {
+            if (m_row < p.M && n0 < p.N) {
                 nchunks = (p.N - n0 + Cfg::EPI_COLS - 1) / Cfg::EPI_COLS;
-                nchunks = nchunks < CHUNKS ? nchunks : CHUNKS;
+                nchunks = nchunks < max_chunks ? nchunks : max_chunks;
             }
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(b * BN);

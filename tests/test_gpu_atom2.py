@@ -73,3 +73,36 @@ def test_atom2_conv(tile_n, out_f32):
     assert tp.tp_last_plan()["atom"] == 2
     ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, st, pad)
     check_against_oracle(host_f64(y), ref, ab, out_f32, "atom2 conv")
+
+
+# ------------------------------------------------------ narrow tail ---
+
+@pytest.mark.parametrize("M,N,K,max_ctas", [(1280, 512, 640, 8),     # 10 tiles on 4 clusters: 8 whole + 4 halves
+                                             (2560, 2048, 384, 0),    # 80 tiles on 76 clusters: 76 + 8 halves
+                                             (600, 100, 448, 0),      # 3 tiles, all halves; upper halves out of N
+                                             (320, 200, 448, 0)])
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_narrow_tail_units(M, N, K, max_ctas, out_f32):
+    A, B = datagen.gemm_operands(M, N, K, seed=M + N)
+    ldc = (N + 7) // 8 * 8
+    got, plan = run_gemm(A, B, M, N, K, K, K, ldc=ldc, out_f32=out_f32, atom=2, tile_n=256, max_ctas=max_ctas)
+    assert plan["tail_units"] > 0
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, out_f32, f"narrow tail {M}x{N}x{K}")
+    got2, plan2 = run_gemm(A, B, M, N, K, K, K, ldc=ldc, out_f32=out_f32, atom=2, tile_n=256, max_ctas=max_ctas,
+                           no_tail=1)
+    assert plan2["tail_units"] == 0
+    check_against_oracle(got2, ref, ab, out_f32, f"whole tiles {M}x{N}x{K}")
+    if out_f32:
+        assert np.array_equal(got, got2)   # same MMAs per output element, same order
+
+
+def test_narrow_tail_conv():
+    N, H, W, C, K, R, S = 4, 20, 18, 64, 256, 3, 3   # 1440 pixels: 6 pair tiles, all halves
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=23)
+    y = new_out(N * H * W, K, False)   # the 2-SM / N 256 conv is compiled with a bf16 output
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, 1, 1, atom=2, tile_n=256)
+    expect_ok()
+    assert tp.tp_last_plan()["tail_units"] == 12
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, 1)
+    check_against_oracle(host_f64(y), ref, ab, False, "conv narrow tail")

@@ -189,3 +189,22 @@ def test_splitk_workspace_arithmetic():
     ks = [k for k in tp.tp_list_kernels() if k["splitk"]]
     assert {(k["atom"], k["tile_n"]) for k in ks} == {(1, 128), (1, 256), (2, 128), (2, 256)}
     assert all(k["out_f32"] == 1 and k["conv"] == 0 for k in ks)
+
+
+def test_narrow_tail_plan():
+    # 8192^3 on 152 SMs: 1024 pair tiles, 76 clusters, 36 left for the last
+    # wave -> 72 half-width units.
+    st, p = plan(8192, 8192, 8192)
+    assert (p["atom"], p["tile_n"], p["tail_units"], p["grid"]) == (2, 256, 72, 152)
+    st, p = plan(8192, 8192, 8192, no_tail=1)
+    assert p["tail_units"] == 0
+    # 10 tiles on 4 clusters: 8 whole, 2 left -> 4 halves.
+    st, p = plan(1280, 512, 640, atom=2, tile_n=256, max_ctas=8)
+    assert (p["tail_units"], p["grid"]) == (4, 8)
+    # No tail when the leftover does not fit twice into a wave, or for N = 128.
+    st, p = plan(2048 * 5, 256 * 16, 512, atom=2, tile_n=256)     # 40 x 16 = 640 tiles: 640 % 76 = 32 fits
+    assert p["tail_units"] == 64
+    st, p = plan(256 * 70, 256, 512, atom=2, tile_n=256)          # 70 tiles < 76 clusters: all halves, 140 > 76
+    assert p["tail_units"] == 0
+    st, p = plan(8192, 8192, 8192, atom=2, tile_n=128)
+    assert p["tail_units"] == 0
