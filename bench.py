@@ -271,6 +271,25 @@ def e2e_pipelined(torch, tp, a_h, b_h, c_h, M, N, K, opts, steps):
     return e0.elapsed_time(e1) / steps
 
 
+def role_timeline(torch, tp, launch):
+    """One traced launch: per-role waiting shares averaged over CTAs (the
+    MMA issuer's over pair leaders)."""
+    launch(None)
+    plan = tp.tp_last_plan()
+    buf = torch.zeros(tp.TRACE_SLOTS * plan["grid"], dtype=torch.int64, device="cuda")
+    launch(buf)
+    torch.cuda.synchronize()
+    t = buf.view(plan["grid"], tp.TRACE_SLOTS).double().cpu()
+    mma = t[::plan["cluster"]]
+    return {
+        "producer_wait_empty_share": round(float((t[:, 1] / t[:, 0]).mean()), 3),
+        "mma_wait_full_share": round(float((mma[:, 3] / mma[:, 2]).mean()), 3),
+        "mma_wait_acc_empty_share": round(float((mma[:, 4] / mma[:, 2]).mean()), 3),
+        "epilogue_wait_acc_full_share": round(float((t[:, 6] / t[:, 5]).mean()), 3),
+        "mma_span_us": round(float(mma[:, 2].mean()) / 1e3, 2),
+    }
+
+
 def measure_rows(torch, tp, stream, peaks, flush_buf):
     """The path's other rows, each with its own roofline."""
     import numpy as np
@@ -299,6 +318,8 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         conv_res[name] = {"us": round(med * 1e3, 2), "tflops": round(flops / (med * 1e-3) / 1e12, 1),
                           "frac_of_peak": round(flops / (med * 1e-3) / 1e12 / peaks["bf16_tflops"], 3),
                           "atom": plan["atom"], "tile_n": plan["tile_n"], "pipe_depth": plan["pipe_depth"]}
+    conv_res["role_timeline"] = role_timeline(
+        torch, tp, lambda tr: tp.tp_conv2d_fprop_bf16_ex(xd, wd, y, N, H, W, C, K, R, S, 1, 1, stream=s, trace=tr))
     rows["conv_32x56x56x256_3x3"] = {"unit": "TFLOP/s", "l2": "flushed between calls", **conv_res}
     del xd, wd, y
 
@@ -321,6 +342,8 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         bound = min(peaks["bf16_tflops"], f / byts * peaks["hbm_gbs"] * 1e9 / 1e12)
         row = {"us": round(med * 1e3, 2), "tflops": round(tfl, 1), "roofline_tflops": round(bound, 1),
                "frac": round(tfl / bound, 3), "grid": tp.tp_last_plan()["grid"]}
+        row["role_timeline"] = role_timeline(
+            torch, tp, lambda tr: tp.tp_gemm_bf16_ex(a, b, c, Ms, Ns, Ks, Ks, Ks, Ns, stream=s, trace=tr))
         # split-K with a caller workspace (slices chosen by the library)
         ws = torch.empty(tp.tp_gemm_splitk_workspace_bytes(Ms, Ns, 16) // 4, dtype=torch.float32, device="cuda")
 
@@ -591,6 +614,8 @@ def tp_arm(args):
 
     rows = sweep = None
     cpu = None
+    timeline = role_timeline(torch, tp, lambda tr: tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, stream=s,
+                                                                       trace=tr, **opts))
     if rank == 0 and not args.no_rows:
         flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
         rows = measure_rows(torch, tp, stream, peaks, flush_buf)
@@ -625,6 +650,7 @@ def tp_arm(args):
                     "serial_value": round(flop * world / (serial_ms * 1e-3) / 1e12, 2)},
             "clocks": clocks,
             "gpu_launches": args.steps,
+            "role_timeline": timeline,
             "rows": rows,
         }
         if sweep is not None:

@@ -98,6 +98,12 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   no_tail:    1 keeps whole tiles in the last wave (the 2-SM, N = 256
  *               variant otherwise runs a partial last wave as half-width
  *               tiles).
+ *   trace:      NULL, or a caller-owned, zeroed device buffer of
+ *               TP_TRACE_SLOTS x (CTAs of the launch, tp_plan.grid) uint64
+ *               that the mainloop fills with its role timeline (below):
+ *               nanoseconds each role spent waiting on each barrier and its
+ *               active span, per CTA (the pair's leader holds the MMA
+ *               issuer's counters). Tracing adds a timer read per wait.
  * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
  * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
  * "StageCount<9> fails the capacity assert"; a combination that fits but is
@@ -111,7 +117,17 @@ typedef struct {
     int max_ctas;
     int l2_hint;
     int no_tail;
+    uint64_t* trace;
 } tp_gemm_opts;
+
+/* Role-timeline counters per CTA (tp_gemm_opts.trace), in this order:
+ * producer span, producer waiting for a free stage, MMA issuer span, MMA
+ * waiting for a loaded stage, MMA waiting for a drained accumulator, epilogue
+ * span (one warp), epilogue waiting for a finished accumulator, work units.
+ * A stage ring that keeps the tensor core fed shows MMA waits that are a
+ * small share of the MMA span ("B200 Tma Pipeline Designer", step 8: copies
+ * genuinely overlapping tensor-core work). */
+#define TP_TRACE_SLOTS 8
 
 /* tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit choices (opts may be NULL).
  * out_f32 selects a float C (1) or a bf16 C (0). */

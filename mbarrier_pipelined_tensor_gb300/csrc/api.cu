@@ -14,6 +14,8 @@
 #include "tensor_map.h"
 #include "tp.h"
 
+static_assert(TP_TRACE_SLOTS == tp::kTraceSlots, "trace layout");
+
 namespace tp {
 const KernelEntry* table_mainloop_cg1(int* n);
 const KernelEntry* table_mainloop_cg2(int* n);
@@ -541,6 +543,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.group_m = group_m_for(opts, pl.m_tiles);
     l2_hints_for(opts, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
+    p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.C = use_splitk ? ws : C;
     p.ldc_bytes = use_splitk ? ldw * 4 : ldc * eb;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};
@@ -705,6 +708,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.conv_S = static_cast<int>(S);
     p.conv_cblocks = static_cast<int>(cblocks);
     p.n_tma = ldg ? 0 : static_cast<int>(K);  // TMA path: K % 8 == 0, rows are whole 16-byte granules
+    p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.C = y;
     p.ldc_bytes = K * eb_out;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};

@@ -114,7 +114,23 @@ struct GemmParams {
     const uint16_t* B;
     int64_t lda, ldb;
     int conv_H, conv_W, conv_C, conv_R;
+    // Optional role timeline: kTraceSlots counters per CTA (nanoseconds,
+    // accumulated with atomicAdd), or nullptr.
+    unsigned long long* trace;
     WaitCtl wait;
+};
+
+// Role-timeline counters, per CTA (GemmParams::trace).
+enum : int {
+    TRACE_PRODUCER_SPAN = 0,      // producer: first wait -> last load issued
+    TRACE_PRODUCER_WAIT_EMPTY,    // producer: waiting for a free stage
+    TRACE_MMA_SPAN,               // MMA issuer: first wait -> last commit
+    TRACE_MMA_WAIT_FULL,          // MMA issuer: waiting for a loaded stage
+    TRACE_MMA_WAIT_ACC_EMPTY,     // MMA issuer: waiting for a drained accumulator
+    TRACE_EPI_SPAN,               // epilogue (one warp): first wait -> last store issued
+    TRACE_EPI_WAIT_ACC_FULL,      // epilogue: waiting for a finished accumulator
+    TRACE_UNITS,                  // work units this CTA's MMA issuer processed
+    kTraceSlots
 };
 
 struct CopyParams {

@@ -184,6 +184,26 @@ __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& 
     return w;
 }
 
+
+
+// Role timeline: adds `v` to this CTA's counter `slot` when tracing is on.
+__device__ __forceinline__ void trace_add(const GemmParams& p, int slot, unsigned long long v)
+{
+    if (p.trace) atomicAdd(p.trace + static_cast<size_t>(blockIdx.x) * kTraceSlots + slot, v);
+}
+
+// Bounded wait that charges its duration to a timeline slot.
+template <bool CL>
+__device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int site, unsigned long long& acc)
+{
+    if (!p.trace) return wait_bounded<CL>(bar, parity, p.wait, abort_flag, site);
+    const uint64_t t0 = globaltimer_ns();
+    const bool ok = wait_bounded<CL>(bar, parity, p.wait, abort_flag, site);
+    acc += globaltimer_ns() - t0;
+    return ok;
+}
+
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
 __global__ void __launch_bounds__(192, 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -287,6 +307,8 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
+            unsigned long long t_wait = 0;
+            const uint64_t t_start = p.trace ? globaltimer_ns() : 0;
             for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
                 const Unit w = unit_of(u, num_tiles, p);
                 int mt, nt;
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(192, 1)
                     base_w = qq * p.conv_stride - p.conv_pad;
                 }
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded<CL>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY)) {
+                    if (!timed_wait<CL>(p, empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY, t_wait)) {
                         ok = false;
                         break;
                     }
@@ -345,6 +367,10 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            if (p.trace) {
+                trace_add(p, TRACE_PRODUCER_SPAN, globaltimer_ns() - t_start);
+                trace_add(p, TRACE_PRODUCER_WAIT_EMPTY, t_wait);
+            }
             if (!ok && (!CL || leader)) {
                 // Gave up: let the loads already in flight land before the
                 // CTA's shared memory can be released (bounded as well).
@@ -373,15 +399,17 @@ __global__ void __launch_bounds__(192, 1)
                 uint32_t ph = 0;
                 int lt = 0;
                 bool ok = true;
+                unsigned long long t_full = 0, t_acc = 0;
+                const uint64_t t_start = p.trace ? globaltimer_ns() : 0;
                 for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++lt) {
                     const Unit w = unit_of(u, num_tiles, p);
                     const int b = lt & 1;
                     const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-                    if (!wait_bounded<CL>(acce_bar(b), aph ^ 1u, p.wait, abort_flag, SITE_MMA_ACC_EMPTY)) break;
+                    if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
                     tcgen05_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!wait_bounded<CL>(full_bar(s), ph, p.wait, abort_flag, SITE_MMA_FULL)) {
+                        if (!timed_wait<CL>(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
                             ok = false;
                             break;
                         }
@@ -406,6 +434,12 @@ __global__ void __launch_bounds__(192, 1)
                     if constexpr (CL) umma_commit_pair(accf_bar(b), 0x3);
                     else umma_commit(accf_bar(b));
                 }
+                if (p.trace) {
+                    trace_add(p, TRACE_MMA_SPAN, globaltimer_ns() - t_start);
+                    trace_add(p, TRACE_MMA_WAIT_FULL, t_full);
+                    trace_add(p, TRACE_MMA_WAIT_ACC_EMPTY, t_acc);
+                    trace_add(p, TRACE_UNITS, static_cast<unsigned long long>(lt));
+                }
                 // Every MMA this thread issued completes before teardown.
                 if constexpr (CL) umma_commit_pair(drain_bar, 0x1);
                 else umma_commit(drain_bar);
@@ -422,11 +456,13 @@ __global__ void __launch_bounds__(192, 1)
         constexpr int CHUNKS = BN / Cfg::EPI_COLS;
         int buf = 0;
         int lt = 0;
+        unsigned long long t_accf = 0;
+        const uint64_t t_start = p.trace ? globaltimer_ns() : 0;
         for (int u = cluster_id; u < num_units; u += num_clusters, ++lt) {
             const Unit w = unit_of(u, num_tiles, p);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-            if (!wait_bounded<CL>(accf_bar(b), aph, p.wait, abort_flag, SITE_EPI_ACC_FULL)) break;
+            if (!timed_wait<CL>(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
             tcgen05_fence_after();
             int mt, nt;
             tile_coords(w.tile, p, mt, nt);
@@ -518,6 +554,10 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+        }
+        if (p.trace && warp == 2 && lane == 0) {
+            trace_add(p, TRACE_EPI_SPAN, globaltimer_ns() - t_start);
+            trace_add(p, TRACE_EPI_WAIT_ACC_FULL, t_accf);
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();

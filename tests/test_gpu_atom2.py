@@ -106,3 +106,25 @@ def test_narrow_tail_conv():
     assert tp.tp_last_plan()["tail_units"] == 12
     ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, 1)
     check_against_oracle(host_f64(y), ref, ab, False, "conv narrow tail")
+
+
+# ------------------------------------------------------- role timeline ---
+
+@pytest.mark.parametrize("atom,tile_n", [(2, 256), (1, 128)])
+def test_role_timeline(atom, tile_n):
+    M, N, K = 2560, 2048, 1024
+    A, B = datagen.gemm_operands(M, N, K, seed=81)
+    a, b = dev_bf16(A), dev_bf16(B)
+    c1, c2 = new_out(M, N, True), new_out(M, N, True)
+    tp.tp_gemm_bf16_ex(a, b, c1, M, N, K, K, K, N, out_f32=True, atom=atom, tile_n=tile_n)
+    plan = tp.tp_last_plan()
+    trace = torch.zeros(tp.TRACE_SLOTS * plan["grid"], dtype=torch.int64, device="cuda")
+    tp.tp_gemm_bf16_ex(a, b, c2, M, N, K, K, K, N, out_f32=True, atom=atom, tile_n=tile_n, trace=trace)
+    expect_ok()
+    assert torch.equal(c1, c2)                                  # tracing does not change results
+    t = trace.view(plan["grid"], tp.TRACE_SLOTS).cpu().numpy()
+    issuers = t[::atom]                                         # the pair's leader issues the MMAs
+    tiles = plan["m_tiles"] * plan["n_tiles"]
+    assert issuers[:, 7].sum() == tiles + plan["tail_units"] // 2  # whole tiles, plus 2 units per tail tile
+    for rows, span, wait in ((t, 0, 1), (issuers, 2, 3), (issuers, 2, 4), (t, 5, 6)):
+        assert np.all(rows[:, span] > 0) and np.all(rows[:, wait] <= rows[:, span])
