@@ -333,6 +333,21 @@ TP_API int tp_list_kernels(tp_kernel_desc* out, int cap);
 TP_API int tp_probe_fma_latency(int kind, int chain, double seed, double* result, double* cycles_per_link,
                                 void* stream);
 
+/*
+ * Failure-detection self test of the real mainloop: runs the 1-SM GEMM
+ * C = A.B (fp32 C, lda = ldb = K, ldc = N) with its producer withholding the
+ * expect_tx arrival of the first stage while still issuing that stage's TMA
+ * loads -- the lost-arrival bug of CUTLASS issue #3722 ("Cause"). The MMA
+ * issuer's bounded wait on that stage, and the waits that depend on it
+ * (epilogue, producer), must give up after limit_ms (1..10000); the first to
+ * expire records TP_ERR_TIMEOUT (site 2 MMA issuer, 4 epilogue, 1 producer),
+ * and the kernel must let its landed loads drain, free tensor memory and return;
+ * tp_device_status then reports the timeout and the context stays usable.
+ * C is left unspecified. Sizes: M, N <= 4096, 64 <= K <= 4096.
+ */
+TP_API int tp_selftest_mainloop_withheld_arrival(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                                 int64_t K, uint32_t limit_ms, void* stream);
+
 /* Launches one CTA that waits on an mbarrier nothing arrives on, with a
  * limit of limit_us microseconds: the wait must give up and record
  * TP_ERR_TIMEOUT, which tp_device_status then returns. Checks that a stuck

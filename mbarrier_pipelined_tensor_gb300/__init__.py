@@ -99,6 +99,7 @@ _SIGS = {
     "tp_last_plan": ([ctypes.POINTER(tp_plan)], _I),
     "tp_list_kernels": ([ctypes.POINTER(tp_kernel_desc), _I], _I),
     "tp_selftest_wait_timeout": ([ctypes.c_uint32, _P], _I),
+    "tp_selftest_mainloop_withheld_arrival": ([_P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P], _I),
     "tp_probe_fma_latency": ([_I, _I, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(ctypes.c_double), _P], _I),
 }
@@ -284,6 +285,11 @@ def tp_probe_fma_latency(kind: int, chain: int = 65536, seed: float = 0.0, strea
     _check(_lib.tp_probe_fma_latency(kind, chain, seed, ctypes.byref(r), ctypes.byref(c), _stream(stream)),
            "tp_probe_fma_latency")
     return r.value, c.value
+
+
+def tp_selftest_mainloop_withheld_arrival(A, B, C, M, N, K, limit_ms, stream=None):
+    _check(_lib.tp_selftest_mainloop_withheld_arrival(_ptr(A), _ptr(B), _ptr(C), M, N, K, limit_ms, _stream(stream)),
+           "tp_selftest_mainloop_withheld_arrival")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None):

@@ -57,6 +57,9 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 thread_local int t_last_cuda_error = 0;
+// Set only inside tp_selftest_mainloop_withheld_arrival for its one launch.
+thread_local int t_selftest_withhold = 0;
+thread_local uint64_t t_selftest_limit_ns = 0;
 thread_local tp_plan t_last_plan = {};
 
 int cuda_fail(cudaError_t e)
@@ -546,7 +549,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.C = use_splitk ? ws : C;
     p.ldc_bytes = use_splitk ? ldw * 4 : ldc * eb;
-    p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    p.wait = WaitCtl{dev->status, t_selftest_limit_ns ? t_selftest_limit_ns : wait_limit_ns()};
+    p.withhold_first_arrival = t_selftest_withhold;
     if (use_splitk) {
         const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
         L.grid = pl.grid;
@@ -916,6 +920,21 @@ int tp_probe_fma_latency(int kind, int chain, double seed, double* result, doubl
     if (e != cudaSuccess) return cuda_fail(e);
     *cycles_per_link = static_cast<double>(cycles) / static_cast<double>(chain);
     return TP_OK;
+}
+
+int tp_selftest_mainloop_withheld_arrival(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                          int64_t K, uint32_t limit_ms, void* stream)
+{
+    if (limit_ms == 0 || limit_ms > 10000 || M > 4096 || N > 4096 || K < 64 || K > 4096) return TP_ERR_INVALID_ARG;
+    tp_gemm_opts o{};
+    o.atom = 1;
+    o.tile_n = 128;
+    t_selftest_withhold = 1;
+    t_selftest_limit_ns = static_cast<uint64_t>(limit_ms) * 1000000ull;
+    const int st = gemm_impl(A, B, C, M, N, K, K, K, N, 1, &o, 0, 0, nullptr, 0, stream);
+    t_selftest_withhold = 0;
+    t_selftest_limit_ns = 0;
+    return st;
 }
 
 int tp_selftest_wait_timeout(uint32_t limit_us, void* stream)

@@ -117,6 +117,10 @@ struct GemmParams {
     // Optional role timeline: kTraceSlots counters per CTA (nanoseconds,
     // accumulated with atomicAdd), or nullptr.
     unsigned long long* trace;
+    // Self-test only (tp_selftest_mainloop_withheld_arrival): 1 makes the
+    // producer withhold the expect_tx arrival of its first stage while still
+    // issuing its loads, so the consumer's bounded wait must give up.
+    int withhold_first_arrival;
     WaitCtl wait;
 };
 

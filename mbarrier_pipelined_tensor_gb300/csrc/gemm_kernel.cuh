@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const uint32_t fb = CL ? mapa_shared(full_bar(s), 0) : full_bar(s);
-                    if (leader) mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
+                    if (leader && !(p.withhold_first_arrival && issued == 0))
+                        mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
                     const uint32_t dA = sA + s * Cfg::A_BYTES;
                     const uint32_t dB = sB + s * Cfg::B_BYTES;
                     if constexpr (CONV) {

@@ -109,6 +109,25 @@ def test_bounded_wait_gives_up_with_status():
     assert torch.equal(src, dst)
 
 
+def test_mainloop_lost_arrival_times_out_and_recovers():
+    # The producer withholds its first stage's expect_tx arrival but issues the
+    # loads (the lost-arrival bug): the MMA issuer's bounded wait must give up,
+    # the kernel must drain and return, and the context must stay usable.
+    M, N, K = 256, 256, 512
+    A, B = datagen.gemm_operands(M, N, K, seed=95)
+    a, b = dev_bf16(A), dev_bf16(B)
+    c = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    tp.tp_selftest_mainloop_withheld_arrival(a, b, c, M, N, K, 200)
+    st, site, block, thread = tp.tp_device_status_detail()
+    # Whichever dependent bounded wait expires first records it: the MMA
+    # issuer's (2), the epilogue's (4) or the producer's (1).
+    assert st == tp.TP_ERR_TIMEOUT and site in (1, 2, 4), (st, site)
+    assert tp.tp_device_status() == tp.TP_OK
+    got, _ = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=1, tile_n=128)
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, True, "after the lost-arrival self test")
+
+
 # ---------------------------------------------------------- GEMM, 1-SM ---
 
 @pytest.mark.parametrize("out_f32", [True, False])
