@@ -128,15 +128,23 @@ def _ptr(x):
     return x.data_ptr()
 
 
+_current_stream = None
+
+
 def _stream(s):
+    """A stream argument as a cudaStream_t integer: an int is passed through,
+    an object with .cuda_stream gives its handle, None means torch's current
+    stream (or the legacy default stream without torch)."""
+    global _current_stream
     if s is None:
-        try:
-            import torch
-            if torch.cuda.is_available():
-                return torch.cuda.current_stream().cuda_stream
-        except ImportError:
-            pass
-        return 0
+        if _current_stream is None:
+            try:
+                import torch
+                _current_stream = (lambda: torch.cuda.current_stream().cuda_stream) \
+                    if torch.cuda.is_available() else (lambda: 0)
+            except ImportError:
+                _current_stream = lambda: 0  # noqa: E731
+        return _current_stream()
     if isinstance(s, int):
         return s
     return s.cuda_stream

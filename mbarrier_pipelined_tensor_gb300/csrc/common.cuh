@@ -2,6 +2,7 @@
 // record, bounded barrier waits and the kernel parameter blocks.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -143,6 +144,23 @@ struct CopyParams {
     uint32_t tile_bytes;
     WaitCtl wait;
 };
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device
+// (the attribute is per function and context; setting it on every launch
+// costs host time a small problem cannot hide). `done` is one bit per device,
+// owned by the caller's kernel instantiation.
+template <typename Kern>
+inline cudaError_t smem_limit_once(Kern kern, int bytes, std::atomic<uint64_t>& done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Key of one compiled GEMM/conv mainloop.
 struct KernelKey {

@@ -99,7 +99,8 @@ cudaError_t launch_tma_copy(const CUtensorMap& s, const CUtensorMap& d, const Co
     const uint32_t stride = (p.tile_bytes + 1023u) & ~1023u;
     const int smem = 1024 + STAGES * static_cast<int>(stride) + 8 * STAGES + 16;
     auto kern = tma_copy_kernel<STAGES, LAG>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = smem_limit_once(kern, 232448, smem_set);  // the limit, not this launch's size
     if (e != cudaSuccess) return e;
     kern<<<grid, 32, smem, st>>>(s, d, p);
     return cudaGetLastError();

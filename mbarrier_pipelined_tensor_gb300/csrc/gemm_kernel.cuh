@@ -578,7 +578,8 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
     auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = smem_limit_once(kern, Cfg::SMEM_BYTES, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);

@@ -50,6 +50,70 @@ uint32_t elem_bytes(CUtensorMapDataType t)
     }
 }
 
+// A small cache of encoded maps (host memory only): a map depends only on its
+// descriptor fields, so repeated calls on the same buffers and shapes reuse it
+// instead of asking the driver again. Round-robin replacement.
+constexpr int kCacheSize = 64;
+
+bool same(const TiledDesc& a, const TiledDesc& b)
+{
+    if (a.dtype != b.dtype || a.rank != b.rank || a.base != b.base || a.swizzle != b.swizzle) return false;
+    for (uint32_t i = 0; i < a.rank; ++i)
+        if (a.dims[i] != b.dims[i] || a.box[i] != b.box[i]) return false;
+    for (uint32_t i = 0; i + 1 < a.rank; ++i)
+        if (a.strides_bytes[i] != b.strides_bytes[i]) return false;
+    return true;
+}
+
+bool same(const Im2colDesc& a, const Im2colDesc& b)
+{
+    if (a.dtype != b.dtype || a.base != b.base || a.swizzle != b.swizzle || a.channels != b.channels ||
+        a.pixels != b.pixels)
+        return false;
+    for (int i = 0; i < 4; ++i)
+        if (a.dims[i] != b.dims[i] || a.elem_strides[i] != b.elem_strides[i]) return false;
+    for (int i = 0; i < 3; ++i)
+        if (a.strides_bytes[i] != b.strides_bytes[i]) return false;
+    for (int i = 0; i < 2; ++i)
+        if (a.lower[i] != b.lower[i] || a.upper[i] != b.upper[i]) return false;
+    return true;
+}
+
+template <typename Desc>
+struct MapCache {
+    struct Entry {
+        Desc key;
+        CUtensorMap map;
+        bool valid;
+    };
+    Entry e[kCacheSize] = {};
+    int next = 0;
+    std::mutex mu;
+
+    bool find(const Desc& d, CUtensorMap* out)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < kCacheSize; ++i)
+            if (e[i].valid && same(e[i].key, d)) {
+                *out = e[i].map;
+                return true;
+            }
+        return false;
+    }
+
+    void put(const Desc& d, const CUtensorMap& m)
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        e[next].key = d;
+        e[next].map = m;
+        e[next].valid = true;
+        next = (next + 1) % kCacheSize;
+    }
+};
+
+MapCache<TiledDesc> g_tiled_cache;
+MapCache<Im2colDesc> g_im2col_cache;
+
 }  // namespace
 
 bool tiled_ok(const TiledDesc& d)
@@ -71,6 +135,7 @@ bool tiled_ok(const TiledDesc& d)
 
 int encode_tiled(CUtensorMap* out, const TiledDesc& d)
 {
+    if (g_tiled_cache.find(d, out)) return ST_OK;
     resolve();
     if (!g_found) return ST_CUDA;
     if (!tiled_ok(d)) return ST_INVALID_ARG;
@@ -79,11 +144,14 @@ int encode_tiled(CUtensorMap* out, const TiledDesc& d)
                          reinterpret_cast<const cuuint64_t*>(d.strides_bytes),
                          reinterpret_cast<const cuuint32_t*>(d.box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          d.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? ST_OK : ST_DRIVER_ENCODE;
+    if (r != CUDA_SUCCESS) return ST_DRIVER_ENCODE;
+    g_tiled_cache.put(d, *out);
+    return ST_OK;
 }
 
 int encode_im2col(CUtensorMap* out, const Im2colDesc& d)
 {
+    if (g_im2col_cache.find(d, out)) return ST_OK;
     resolve();
     if (!g_found) return ST_CUDA;
     if ((reinterpret_cast<uintptr_t>(d.base) & 15u) != 0) return ST_INVALID_ARG;
@@ -94,7 +162,9 @@ int encode_im2col(CUtensorMap* out, const Im2colDesc& d)
                           d.pixels, reinterpret_cast<const cuuint32_t*>(d.elem_strides),
                           CU_TENSOR_MAP_INTERLEAVE_NONE, d.swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? ST_OK : ST_DRIVER_ENCODE;
+    if (r != CUDA_SUCCESS) return ST_DRIVER_ENCODE;
+    g_im2col_cache.put(d, *out);
+    return ST_OK;
 }
 
 }  // namespace tp

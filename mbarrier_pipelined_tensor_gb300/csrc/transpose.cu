@@ -142,7 +142,8 @@ cudaError_t launch_tma_transpose_t(const CUtensorMap& s, const CUtensorMap& d, c
 {
     const int smem = transpose_smem_bytes(STAGES);
     auto kern = tma_transpose_kernel<STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = smem_limit_once(kern, smem, smem_set);  // fixed per instantiation
     if (e != cudaSuccess) return e;
     kern<<<grid, 32, smem, st>>>(s, d, p);
     return cudaGetLastError();
