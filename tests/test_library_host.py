@@ -208,3 +208,23 @@ def test_narrow_tail_plan():
     assert p["tail_units"] == 0
     st, p = plan(8192, 8192, 8192, atom=2, tile_n=128)
     assert p["tail_units"] == 0
+
+
+def test_no_tma_multicast_in_kernels():
+    """The 2-SM atom feeds each CTA of the pair from its own TMA loads, which
+    complete on the leader's barrier ("SM100_TMA_2SM_LOAD" semantics: each
+    CTA loads its half, no multicast). No bulk-copy instruction in the kernel
+    sources carries a cluster multicast; the one multicast token allowed is
+    the tensor-core commit that signals both CTAs of the pair."""
+    csrc = os.path.join(ROOT, "mbarrier_pipelined_tensor_gb300", "csrc")
+    offenders = []
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            continue
+        with open(os.path.join(csrc, name)) as f:
+            for n, line in enumerate(f, 1):
+                if "multicast" not in line:
+                    continue
+                if re.search(r"cp\.async\.bulk|\.tile::|im2col", line) or "tcgen05.commit" not in line:
+                    offenders.append(f"{name}:{n}: {line.strip()}")
+    assert not offenders, offenders
