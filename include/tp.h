@@ -94,7 +94,12 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM).
  *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
  *               1 none, 2 A evict-last / B evict-first, 3 A evict-last,
- *               4 B evict-first.
+ *               4 B evict-first, 5 A evict-first / B evict-last, 6 B
+ *               evict-last. "Choose" (GEMM only; the convolution keeps 1)
+ *               picks 2 when at most two tile rows read B and A is small
+ *               (<= 16 MB, under a quarter of B): B then streams through L2
+ *               once while A, read by every tile, stays. It picks 5 in the
+ *               mirrored case, else 1.
  *   no_tail:    1 keeps whole tiles in the last wave (the 2-SM, N = 256
  *               variant otherwise runs a partial last wave as half-width
  *               tiles).
@@ -295,6 +300,7 @@ typedef struct {
     int64_t m_tiles, n_tiles, k_blocks;
     int splits;      /* K slices (1 unless split-K ran) */
     int tail_units;  /* half-width units of the last wave (0: none) */
+    int l2_hint;     /* operand L2 priorities used (tp_gemm_opts.l2_hint 1-6) */
 } tp_plan;
 
 /*

@@ -59,7 +59,8 @@ class tp_plan(ctypes.Structure):
                 ("tile_n", ctypes.c_int), ("out_f32", ctypes.c_int), ("conv", ctypes.c_int),
                 ("grid", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
-                ("splits", ctypes.c_int), ("tail_units", ctypes.c_int)]
+                ("splits", ctypes.c_int), ("tail_units", ctypes.c_int),
+                ("l2_hint", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -186,11 +186,17 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
         // as half-width units: after at least one full wave it counts half.
         const int64_t r = tiles % clusters;
         if (c.atom == 2 && c.tile_n == 256 && tiles >= clusters && r > 0 && 2 * r <= clusters) waves -= 0.5;
-        double cost = waves * c.tile_n / c.eff;
+        // Estimated time (ns): one k-block of a 128 x tile_n tile is 1.31 *
+        // tile_n ns at one SM's dense BF16 rate, scaled by the variant's
+        // measured efficiency.
+        double cost = waves * static_cast<double>(k_blocks) * 1.31 * c.tile_n / c.eff;
         // Short K: a narrow tile's fixed per-tile cost (ring fill, epilogue)
         // is a larger share of its work (4096 x 4096 x 512: N = 128 tiles
         // measured 27 us against 23 us for N = 256).
         if (k_blocks <= 16 && c.tile_n == 128) cost *= 1.25;
+        // A cluster launch and its pair barriers cost about 2 us more per
+        // call than the 1-SM atom (a one-tile GEMM: 10.9 against 8.9 us).
+        if (c.atom == 2) cost += 2000.0;
         if (!have || cost < best) {
             best = cost;
             pick = c;
@@ -309,16 +315,33 @@ int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
 }
 
 // L2 priorities of the A / B loads (0 normal, 1 evict first, 2 evict last).
-void l2_hints_for(const tp_gemm_opts* o, int* a, int* b)
+// Chosen (l2_hint 0, GEMM) from how often each operand is read: B, read by
+// at most two tile rows, streams through L2 once and goes first, while a
+// small A, read by every tile of the row, is kept; likewise mirrored. The
+// convolution's A is an im2col view that overlapping windows re-read from
+// L2, so it keeps normal priority.
+int l2_mode_for(const tp_gemm_opts* o, int64_t m_tiles, int64_t n_tiles, double a_bytes, double b_bytes, bool gemm)
 {
     const int h = o ? o->l2_hint : 0;
+    if (h != 0) return h;
+    if (!gemm) return 1;
+    constexpr double kKeep = 16.0e6;
+    if (m_tiles <= 2 && a_bytes <= kKeep && 4.0 * a_bytes <= b_bytes) return 2;
+    if (n_tiles <= 2 && b_bytes <= kKeep && 4.0 * b_bytes <= a_bytes) return 5;
+    return 1;
+}
+
+void l2_hints_for(int mode, int* a, int* b)
+{
     *a = 0;
     *b = 0;
-    switch (h) {
+    switch (mode) {
     case 2: *a = 2; *b = 1; break;
     case 3: *a = 2; break;
     case 4: *b = 1; break;
-    default: break;  // 0 (choose) and 1 (none): normal priority
+    case 5: *a = 1; *b = 2; break;
+    case 6: *b = 2; break;
+    default: break;  // 1: normal priority
     }
 }
 
@@ -341,13 +364,17 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u ||
         reinterpret_cast<uintptr_t>(C) % eb)
         return TP_ERR_INVALID_ARG;
-    // TMA suitability: 16-byte aligned bases and byte pitches; otherwise the
-    // plain-load producer feeds the same mainloop.
-    const int ldg = (!aligned16(A) || !aligned16(B) || !aligned16(C) || (lda * 2) % 16 || (ldb * 2) % 16 ||
-                     (ldc * eb) % 16)
-                        ? 1
-                        : 0;
-    return plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl);
+    // TMA suitability of the operands: 16-byte aligned bases and byte
+    // pitches; otherwise the plain-load producer feeds the same mainloop. C
+    // does not decide it: a C that TMA cannot store is written with plain
+    // stores by the epilogue.
+    const int ldg = (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16) ? 1 : 0;
+    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 6)) return TP_ERR_INVALID_ARG;
+    const int st = plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl);
+    if (st == TP_OK)
+        pl->l2_hint = l2_mode_for(opts, pl->m_tiles, pl->n_tiles, 2.0 * static_cast<double>(M) * static_cast<double>(K),
+                                  2.0 * static_cast<double>(N) * static_cast<double>(K), true);
+    return st;
 }
 
 int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
@@ -506,7 +533,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     // last full granule, the epilogue stores the rest (all of C when the
     // plain-load path runs). Split-K partials go to the workspace, whose rows
     // are whole granules.
-    const int64_t n_tma = use_splitk ? ldw : (ldg ? 0 : N / (16 / eb) * (16 / eb));
+    const bool c_tma = aligned16(C) && (ldc * eb) % 16 == 0;
+    const int64_t n_tma = use_splitk ? ldw : (ldg || !c_tma ? 0 : N / (16 / eb) * (16 / eb));
     if (!ldg) {
         TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
                      {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
@@ -521,11 +549,15 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
                          {static_cast<uint64_t>(ldw) * 4, static_cast<uint64_t>(M * ldw) * 4},
                          {32, 32, 1}, CU_TENSOR_MAP_SWIZZLE_128B};
             if ((st = encode_tiled(&L.mapC, dw))) return st;
-        } else {
+        } else if (c_tma) {
             TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
                          {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
                          {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
             if ((st = encode_tiled(&L.mapC, dc))) return st;
+        } else {
+            // n_tma = 0: the epilogue writes all of C with plain stores and
+            // never uses its map, which stays a valid copy of A's.
+            L.mapC = L.mapA;
         }
     }
     GemmParams& p = L.params;
@@ -544,7 +576,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     if (!use_splitk && !(opts && opts->no_tail))
         set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
     p.group_m = group_m_for(opts, pl.m_tiles);
-    l2_hints_for(opts, &p.l2_a, &p.l2_b);
+    l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.C = use_splitk ? ws : C;
@@ -640,11 +672,12 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     // im2col TMA limits (cuTensorMapEncodeIm2col: rank-4 corners in
     // [-128, 127], traversal strides <= 8) and 16-byte byte strides;
     // otherwise the plain-load producer gathers the same tiles.
-    const int ldg = (C % 8 || K % 8 || !aligned16(x) || !aligned16(w) || !aligned16(y) || stride > 8 || R > 32 ||
-                     S > 32 || pad > 127)
-                        ? 1
-                        : 0;
+    const int ldg = (C % 8 || !aligned16(x) || !aligned16(w) || stride > 8 || R > 32 || S > 32 || pad > 127) ? 1 : 0;
+    // y rows of whole 16-byte granules at a 16-byte aligned base go out by
+    // TMA; otherwise the epilogue writes y with plain stores.
+    const bool y_tma = aligned16(y) && (K * eb_out) % 16 == 0;
     const int64_t cblocks = cdiv(C, 64);
+    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 6)) return TP_ERR_INVALID_ARG;
     st = plan_mainloop(M, K, R * S * cblocks, out_f32, 1, ldg, opts, dev->sm_count, &pl);
     if (st) return st;
     const int cg = pl.atom;
@@ -684,8 +717,12 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     TiledDesc dy{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y,
                  {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
                  {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
-    if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw)) || (st = encode_tiled(&L.mapC, dy)))
-        return st;
+    if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw))) return st;
+    if (y_tma) {
+        if ((st = encode_tiled(&L.mapC, dy))) return st;
+    } else {
+        L.mapC = L.mapB;  // never stored through (n_tma = 0)
+    }
     }
     GemmParams& p = L.params;
     p.A = static_cast<const uint16_t*>(x);
@@ -704,14 +741,15 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.kb_per_split = p.k_blocks;
     if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
     p.group_m = group_m_for(opts, pl.m_tiles);
-    l2_hints_for(opts, &p.l2_a, &p.l2_b);
+    pl.l2_hint = l2_mode_for(opts, pl.m_tiles, pl.n_tiles, 0.0, 0.0, false);
+    l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.conv_P = static_cast<int>(P);
     p.conv_Q = static_cast<int>(Q);
     p.conv_stride = static_cast<int>(stride);
     p.conv_pad = static_cast<int>(pad);
     p.conv_S = static_cast<int>(S);
     p.conv_cblocks = static_cast<int>(cblocks);
-    p.n_tma = ldg ? 0 : static_cast<int>(K);  // TMA path: K % 8 == 0, rows are whole 16-byte granules
+    p.n_tma = (ldg || !y_tma) ? 0 : static_cast<int>(K);  // TMA stores: rows are whole 16-byte granules
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.C = y;
     p.ldc_bytes = K * eb_out;

@@ -263,6 +263,13 @@ __global__ void __launch_bounds__(192, 1)
     if constexpr (CL) cluster_sync(); else __syncthreads();
     tcgen05_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The setup above may overlap the tail of the kernel launched before
+    // this one on the stream (programmatic dependent launch); global memory
+    // is touched only after that kernel has completed. From here on, the
+    // kernel queued behind this one may be scheduled (the split-K
+    // reduction, which waits for this grid's end in the same way).
+    griddep_wait();
+    griddep_launch_dependents();
 
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_units = p.tail_units > 0 ? p.n_full + p.tail_units : num_tiles * p.splits;
@@ -586,13 +593,15 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.params);
 }
 

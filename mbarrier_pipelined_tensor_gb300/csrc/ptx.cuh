@@ -140,6 +140,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m)
 
 // L2 eviction priority for a TMA load: 0 normal, 1 evict first (streamed
 // once), 2 evict last (re-read by later tile waves).
+// Programmatic dependent launch. griddep_wait: block until the grids this
+// one was launched behind have completed and their memory writes are
+// visible (returns at once when there are none). griddep_launch_dependents:
+// grids launched behind this one may be scheduled once every CTA of this
+// grid has executed it or exited; they still wait for this grid's end
+// before touching its results.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t make_l2_policy(int kind)
 {
     uint64_t p;

@@ -270,6 +270,58 @@ def test_conv_fallback_producer(case):
     check_against_oracle(host_f64(y), ref, ab, True, f"conv fallback {case}")
 
 
+@pytest.mark.parametrize("atom,tile_n", [(1, 128), (2, 256)])
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_gemm_c_without_tma_stores(atom, tile_n, out_f32):
+    # A and B suit TMA, C does not (base off by one element, odd pitch): the
+    # TMA producer runs and the epilogue writes all of C with plain stores.
+    M, N, K, ldc, oc = 300, 203, 448, 205, 1
+    A, B = datagen.gemm_operands(M, N, K, seed=54)
+    c_all = new_out(1, M * ldc + oc, out_f32).reshape(-1)
+    c = c_all[oc:]
+    tp.tp_gemm_bf16_ex(dev_bf16(A), dev_bf16(B), c, M, N, K, K, K, ldc, out_f32=out_f32, atom=atom, tile_n=tile_n)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_MAINLOOP
+    full = host_f64(c_all)
+    assert np.isnan(full[0])
+    got = full[oc:].reshape(M, ldc)
+    assert np.all(np.isnan(got[:, N:]))
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got[:, :N], ref, ab, out_f32, "C by plain stores")
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_splitk_into_unaligned_c(out_f32):
+    # The reduction's scalar stores: C off by one element, odd pitch.
+    M, N, K, ldc, oc = 128, 331, 2048, 333, 1
+    A, B = datagen.gemm_operands(M, N, K, seed=55)
+    ws = torch.empty(tp.tp_gemm_splitk_workspace_bytes(M, N, 4) // 4, dtype=torch.float32, device="cuda")
+    c_all = new_out(1, M * ldc + oc, out_f32).reshape(-1)
+    tp.tp_gemm_bf16_splitk(dev_bf16(A), dev_bf16(B), c_all[oc:], M, N, K, K, K, ldc, out_f32=out_f32, splits=4,
+                           workspace=ws)
+    expect_ok()
+    assert tp.tp_last_plan()["splits"] == 4
+    full = host_f64(c_all)
+    got = full[oc:].reshape(M, ldc)
+    assert np.isnan(full[0]) and np.all(np.isnan(got[:, N:]))
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got[:, :N], ref, ab, out_f32, "split-K unaligned C")
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_conv_output_channels_not_granular(out_f32):
+    # K = 100 output channels: y rows are not whole 16-byte granules, so y is
+    # written with plain stores while x and w still load through TMA.
+    N, H, W, C, K, R, S = 2, 10, 9, 64, 100, 3, 3
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=56)
+    y = new_out(N * H * W, K, out_f32)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, 1, 1, out_f32=out_f32)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_MAINLOOP
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, 1)
+    check_against_oracle(host_f64(y), ref, ab, out_f32, "conv K=100")
+
+
 def test_fallback_matches_tma_path_bit_for_bit():
     # The same operands through both producers: the tensor core sees the same
     # swizzled stages, so the outputs are identical.

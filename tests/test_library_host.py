@@ -125,9 +125,15 @@ def test_auto_variant_choice():
     # Large square: the 2-SM atom at MMA N = 256 (fewest waves x widest tile).
     st, p = plan(8192, 8192, 8192)
     assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (2, 256, 6)
-    # Few output tiles: N = 128 tiles spread the work over more SMs.
+    # Few output tiles: N = 128 tiles spread the work over more SMs, and a
+    # single wave of 1-SM tiles avoids the cluster's fixed cost.
     st, p = plan(1000, 1000, 1000, lda=1008, ldb=1008, ldc=1000, out_f32=True)
-    assert (p["atom"], p["tile_n"]) == (2, 128) and p["grid"] == 64
+    assert (p["atom"], p["tile_n"]) == (1, 128) and p["grid"] == 64
+    st, p = plan(128, 128, 64)
+    assert (p["atom"], p["tile_n"], p["grid"]) == (1, 128, 1)
+    # Several waves: the 2-SM atom's deeper ring wins.
+    st, p = plan(2560, 2560, 2560)
+    assert (p["atom"], p["tile_n"]) == (2, 256)
     # A fixed field restricts the choice.
     st, p = plan(8192, 8192, 8192, atom=1)
     assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 256, 4)
@@ -164,7 +170,9 @@ def test_plan_tma_suitability():
     assert plan(64, 64, 64, A=AL + 2)[1]["path"] == FB                # base not 16-B aligned
     assert plan(64, 64, 60, lda=60)[1]["path"] == FB                  # lda*2 = 120 not a multiple of 16
     assert plan(64, 60, 64, ldc=60, out_f32=True)[1]["path"] == ML    # 60*4 = 240 = 15*16
-    assert plan(64, 60, 64, ldc=60)[1]["path"] == FB                  # 60*2 = 120
+    assert plan(64, 60, 64, ldc=60)[1]["path"] == ML                  # 60*2 = 120: C by plain stores
+    assert plan(64, 64, 64, C=AL + 2)[1]["path"] == ML                # C base: plain stores, TMA loads
+    assert plan(64, 64, 64, B=AL + 2)[1]["path"] == FB
     st, p = plan(64, 64, 64, A=AL + 2)
     assert st == tp.TP_OK and (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 128, 6)
     assert plan(64, 64, 64, A=AL + 1)[0] == tp.TP_ERR_INVALID_ARG     # a bf16 must be 2-byte aligned
@@ -228,3 +236,21 @@ def test_no_tma_multicast_in_kernels():
                 if re.search(r"cp\.async\.bulk|\.tile::|im2col", line) or "tcgen05.commit" not in line:
                     offenders.append(f"{name}:{n}: {line.strip()}")
     assert not offenders, offenders
+
+
+def test_l2_priority_choice():
+    """Automatic L2 priorities: an operand read by at most two tile rows
+    streams (evict-first) while the small, widely re-read one stays
+    (evict-last); square problems keep normal priority."""
+    def mode(M, N, K, **o):
+        st, p = plan(M, N, K, **o)
+        assert st == tp.TP_OK
+        return p["l2_hint"]
+    assert mode(128, 8192, 16384) == 2      # B streams, A (4 MB) stays
+    assert mode(8192, 128, 16384) == 5      # mirrored
+    assert mode(8192, 8192, 8192) == 1
+    assert mode(4096, 4096, 512) == 1
+    assert mode(128, 256, 64) == 1          # B not much bigger than A
+    assert mode(128, 8192, 16384, l2_hint=1) == 1
+    assert mode(8192, 8192, 8192, l2_hint=4) == 4
+    assert plan(128, 128, 128, l2_hint=7)[0] == tp.TP_ERR_INVALID_ARG
