@@ -59,6 +59,11 @@ def parse_args():
     ap.add_argument("--copy-rows", type=int, default=32768, help="rows (x 16384) for --only copy/transpose")
     ap.add_argument("--gsweep", type=str, default="",
                     help="comma-separated group_m[:l2_hint] values: time a --steps loop of each")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV", default=None,
+                    help="no GPU: write profiles/traffic.json from an ncu --csv capture of the headline launch")
+    ap.add_argument("--traffic-command", default="", help="the ncu command line recorded with --record-traffic")
+    ap.add_argument("--launch-table", metavar="NCU_CSV", default=None,
+                    help="no GPU: print per-kernel launches, total time and share of an ncu --csv launch list")
     return ap.parse_args()
 
 
@@ -661,8 +666,89 @@ def tp_arm(args):
     return 0
 
 
+# ------------------------------------------------------- ncu summaries --
+
+_NCU_UNITS = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+              "nsecond": 1e-9, "ns": 1e-9, "usecond": 1e-6, "us": 1e-6, "msecond": 1e-3, "ms": 1e-3,
+              "second": 1.0, "s": 1.0}
+
+
+def ncu_csv_rows(path):
+    """(launch id, kernel name, metric, value in bytes or seconds) for every
+    metric row of an `ncu --csv` log."""
+    import csv
+    rows, hdr = [], None
+    with open(path, newline="") as f:
+        for r in csv.reader(f):
+            if not r:
+                continue
+            if r[0] == "ID":
+                hdr = r
+                continue
+            if hdr is None or len(r) != len(hdr):
+                continue
+            d = dict(zip(hdr, r))
+            try:
+                v = float(d["Metric Value"].replace(",", ""))
+            except ValueError:
+                continue
+            rows.append((int(d["ID"]), d["Kernel Name"], d["Metric Name"],
+                         v * _NCU_UNITS.get(d.get("Metric Unit", ""), 1.0)))
+    return rows
+
+
+def record_traffic(csv_path, command):
+    """profiles/traffic.json from the last captured mainloop launch."""
+    per = {}
+    for lid, name, metric, v in ncu_csv_rows(csv_path):
+        if "mainloop_kernel" in name:
+            per.setdefault(lid, {"name": name})[metric] = v
+    if not per:
+        raise SystemExit(f"no mainloop_kernel launch in {csv_path}")
+    e = per[max(per)]
+    rd, wr = e["dram__bytes_read.sum"], e["dram__bytes_write.sum"]
+    rec = {"mainloop_kernel": {
+        "source_hash": kernel_source_hash(),
+        "dram_bytes_per_launch": int(round(rd + wr)),
+        "dram_bytes_read": int(round(rd)),
+        "dram_bytes_write": int(round(wr)),
+        "duration_us": round(e.get("gpu__time_duration.sum", 0.0) * 1e6, 2),
+        "variant": e["name"].split("(")[0].replace("void ", ""),
+        "workload": "bf16 GEMM 8192^3 (bench.py default headline)",
+        "command": command,
+        "passes": 1}}
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps(rec))
+
+
+def launch_table(csv_path):
+    """Markdown table: launches, total device time and share per kernel."""
+    tot = {}
+    cnt = {}
+    for _, name, metric, v in ncu_csv_rows(csv_path):
+        if metric != "gpu__time_duration.sum":
+            continue
+        k = name.split("(")[0].replace("void ", "")
+        tot[k] = tot.get(k, 0.0) + v
+        cnt[k] = cnt.get(k, 0) + 1
+    total = sum(tot.values()) or 1.0
+    print("| launches | total ms | share | kernel |")
+    print("|---:|---:|---:|---|")
+    for k in sorted(tot, key=lambda x: -tot[x]):
+        print(f"| {cnt[k]} | {tot[k] * 1e3:.3f} | {100.0 * tot[k] / total:.2f}% | `{k}` |")
+
+
 def main():
     args = parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic, args.traffic_command)
+        return 0
+    if args.launch_table:
+        launch_table(args.launch_table)
+        return 0
     if args.impl == "reference":
         return reference_arm(args)
     return tp_arm(args)
