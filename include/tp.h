@@ -194,6 +194,31 @@ TP_API int tp_gemm_bf16_splitk_noalloc(const void* A, const void* B, void* C, in
 TP_API int64_t tp_gemm_splitk_noalloc_capacity(void);
 
 /*
+ * tp_gemm_bf16_ex on operands in host memory, end to end on `stream`: copies
+ * A (M rows) and B (N rows) into the caller's device buffers dA and dB,
+ * runs the GEMM into the caller's device buffer dC, and copies C back into
+ * C_host. Host and device buffers have the same layout and pitches (lda,
+ * ldb, ldc elements; A, B bf16; C bf16 or fp32 by out_f32), so dA holds
+ * M x lda, dB N x ldb and dC M x ldc elements. The pages define only the
+ * device-resident GEMM; this is its form for callers whose data lives on
+ * the host (the end-to-end measurement uses it).
+ *
+ * Ownership: every buffer is the caller's. The call only enqueues work. C_host
+ * is valid after `stream` has been synchronized, and no buffer may be reused
+ * before then. Host buffers should be page-locked (cudaHostAlloc), so that
+ * the copies run asynchronously on the copy engines; pageable memory works,
+ * but those copies block the host.
+ *
+ * Errors: TP_ERR_INVALID_ARG for negative sizes, pitches below the row
+ * length or NULL buffers; TP_ERR_CUDA when a copy cannot be enqueued (its
+ * code via tp_last_cuda_error); otherwise the statuses of tp_gemm_bf16_ex.
+ * M == 0 or N == 0 is a no-op; K == 0 copies nothing in and returns zeros.
+ */
+TP_API int tp_gemm_bf16_host(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, int out_f32, void* dA, void* dB, void* dC,
+                             const tp_gemm_opts* opts, void* stream);
+
+/*
  * Forward convolution as an implicit GEMM on the same mainloop; the A tile is
  * an im2col TMA load ("two-free-pipeline-stages": SM100_TMA_2SM_LOAD_IM2COL).
  * Cross-correlation, zero padding, no dilation, no groups:

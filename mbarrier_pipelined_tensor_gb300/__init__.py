@@ -80,6 +80,7 @@ _SIGS = {
     "tp_gemm_bf16": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
     "tp_gemm_bf16_f32": ([_P, _P, _P] + [_I64] * 6 + [_P], _I),
     "tp_gemm_bf16_ex": ([_P, _P, _P] + [_I64] * 6 + [_I, ctypes.POINTER(tp_gemm_opts), _P], _I),
+    "tp_gemm_bf16_host": ([_P, _P, _P] + [_I64] * 6 + [_I, _P, _P, _P, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_gemm_bf16_splitk": ([_P, _P, _P] + [_I64] * 6 + [_I, _I, _P, _I64, ctypes.POINTER(tp_gemm_opts), _P], _I),
     "tp_gemm_splitk_workspace_bytes": ([_I64, _I64, _I, ctypes.POINTER(_I64)], _I),
     "tp_gemm_bf16_splitk_noalloc": ([_P, _P, _P] + [_I64] * 6 + [_I, _I, _P], _I),
@@ -199,6 +200,17 @@ def tp_gemm_splitk_workspace_bytes(M, N, splits) -> int:
     b = _I64()
     _check(_lib.tp_gemm_splitk_workspace_bytes(M, N, splits, ctypes.byref(b)), "tp_gemm_splitk_workspace_bytes")
     return int(b.value)
+
+
+def tp_gemm_bf16_host(A_host, B_host, C_host, M, N, K, lda, ldb, ldc, dA, dB, dC, out_f32=False, stream=None,
+                      **opts):
+    """End-to-end GEMM on host operands: upload into the device buffers dA,
+    dB, GEMM into dC, download into C_host, all enqueued on `stream`. Host
+    arguments are pinned torch tensors or raw addresses."""
+    o = _opts(**opts)
+    _check(_lib.tp_gemm_bf16_host(_ptr(A_host), _ptr(B_host), _ptr(C_host), M, N, K, lda, ldb, ldc,
+                                  int(bool(out_f32)), _ptr(dA), _ptr(dB), _ptr(dC), ctypes.byref(o),
+                                  _stream(stream)), "tp_gemm_bf16_host")
 
 
 def tp_gemm_bf16_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, splits=0, stream=None):

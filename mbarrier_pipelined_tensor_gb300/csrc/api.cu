@@ -1035,6 +1035,33 @@ int noalloc_workspace(float** out)
 
 extern "C" {
 
+int tp_gemm_bf16_host(const void* A_host, const void* B_host, void* C_host, int64_t M, int64_t N, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t ldc, int out_f32, void* dA, void* dB, void* dC,
+                      const tp_gemm_opts* opts, void* stream)
+{
+    std::memset(&t_last_plan, 0, sizeof(t_last_plan));
+    if (M < 0 || N < 0 || K < 0) return TP_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TP_OK;
+    if (lda < K || ldb < K || ldc < N) return TP_ERR_INVALID_ARG;
+    if (!C_host || !dC || (K > 0 && (!A_host || !B_host || !dA || !dB))) return TP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t eb = out_f32 ? 4 : 2;
+    cudaError_t e = cudaSuccess;
+    if (K > 0) {
+        e = cudaMemcpy2DAsync(dA, static_cast<size_t>(lda) * 2, A_host, static_cast<size_t>(lda) * 2,
+                              static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dB, static_cast<size_t>(ldb) * 2, B_host, static_cast<size_t>(ldb) * 2,
+                                  static_cast<size_t>(K) * 2, static_cast<size_t>(N), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const int st = gemm_impl(dA, dB, dC, M, N, K, lda, ldb, ldc, out_f32, opts, 0, 0, nullptr, 0, stream);
+    if (st) return st;
+    e = cudaMemcpy2DAsync(C_host, static_cast<size_t>(ldc) * eb, dC, static_cast<size_t>(ldc) * eb,
+                          static_cast<size_t>(N) * eb, static_cast<size_t>(M), cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
 int tp_gemm_bf16_splitk_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                                 int64_t lda, int64_t ldb, int64_t ldc, int out_f32, int splits, void* stream)
 {

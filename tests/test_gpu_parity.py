@@ -389,3 +389,47 @@ def test_fma_chain_latency_probe(kind, floor, ceiling):
     assert result == seed + chain
     assert 1.0 <= cpl <= ceiling
     print(f"kind {kind}: {cpl:.2f} cycles per dependent fma (B200 note: {floor})")
+
+
+# ------------------------------------------------ host-buffer end to end ---
+
+def _pinned(arr):
+    t = torch.from_numpy(np.ascontiguousarray(arr))
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_gemm_host_buffers_end_to_end(out_f32):
+    M, N, K, lda, ldb, ldc = 300, 200, 448, 456, 464, 208    # pitched, ragged tiles
+    A, B = datagen.gemm_operands(M, N, K, seed=57, lda=lda, ldb=ldb)
+    a_h, b_h = _pinned(A.view(np.int16)), _pinned(B.view(np.int16))
+    c_h = torch.full((M, ldc), -1, dtype=torch.int32 if out_f32 else torch.int16).pin_memory()
+    dA = torch.empty(M * lda, dtype=torch.int16, device="cuda")
+    dB = torch.empty(N * ldb, dtype=torch.int16, device="cuda")
+    dC = torch.empty((M, ldc), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    tp.tp_gemm_bf16_host(a_h, b_h, c_h, M, N, K, lda, ldb, ldc, dA, dB, dC, out_f32=out_f32)
+    torch.cuda.synchronize()
+    expect_ok()
+    raw = c_h.numpy()
+    got = (raw.view(np.float32) if out_f32 else datagen.bf16_to_f32(raw.view(np.uint16))).astype(np.float64)
+    assert np.all(raw[:, N:] == -1)                  # the pitch padding is not written
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    check_against_oracle(got[:, :N], ref, ab, out_f32, "host buffers")
+    # The same kernels as the device-resident call: identical bits.
+    c_dev = new_out(M, ldc, out_f32)
+    tp.tp_gemm_bf16_ex(dA.view(torch.bfloat16), dB.view(torch.bfloat16), c_dev, M, N, K, lda, ldb, ldc,
+                       out_f32=out_f32)
+    dev = host_f64(c_dev)
+    assert np.array_equal(dev[:, :N], got[:, :N])
+
+
+def test_gemm_host_buffers_k0_and_errors():
+    M, N = 5, 9
+    c_h = torch.full((M, N), 7.0, dtype=torch.float32).pin_memory()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tp.tp_gemm_bf16_host(None, None, c_h, M, N, 0, 0, 0, N, None, None, dC, out_f32=True)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c_h) == 0
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_gemm_bf16_host(None, None, c_h, M, N, 4, 4, 4, N, None, None, dC, out_f32=True)
+    assert e.value.status == tp.TP_ERR_INVALID_ARG
