@@ -499,11 +499,14 @@ __global__ void __launch_bounds__(192, 1)
                 if constexpr (OUT_F32) {
                     tmem_ld_32x32b_x32(t_row + c * 32, packed);
                     tmem_wait_ld();
+                    tmem_regs_ready(packed);
                 } else {
                     uint32_t v0[32], v1[32];
                     tmem_ld_32x32b_x32(t_row + c * 64, v0);
                     tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
                     tmem_wait_ld();
+                    tmem_regs_ready(v0);
+                    tmem_regs_ready(v1);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         packed[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
