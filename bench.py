@@ -284,6 +284,41 @@ def role_timeline(torch, tp, launch):
     }
 
 
+def small_gemm_latency(torch, tp, stream, reps=50):
+    """us per launch of small GEMMs issued back to back, eagerly and as
+    one replayed CUDA graph of `reps` launches."""
+    import numpy as np
+    import datagen
+    out = {"unit": "us per launch", "launches": reps}
+    for (M, N, K, f32) in ((320, 200, 448, True), (1000, 1000, 1000, False), (4096, 4096, 512, False)):
+        A, B = datagen.gemm_operands(M, N, K, seed=0)
+        lda = (K + 7) // 8 * 8
+        if lda != K:
+            A, B = datagen.pad_rows(A, lda), datagen.pad_rows(B, lda)
+        a = torch.from_numpy(A.view(np.int16)).cuda().view(torch.bfloat16)
+        b = torch.from_numpy(B.view(np.int16)).cuda().view(torch.bfloat16)
+        c = torch.empty((M, N), dtype=torch.float32 if f32 else torch.bfloat16, device="cuda")
+        side = torch.cuda.Stream()
+
+        def launch(st):
+            tp.tp_gemm_bf16_ex(a, b, c, M, N, K, lda, lda, N, out_f32=f32, stream=st.cuda_stream)
+
+        for _ in range(3):
+            launch(side)
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(reps):
+                launch(side)
+        g.replay()
+        torch.cuda.synchronize()
+        eager_ms = time_loop(torch, stream, lambda: launch(stream), reps) / reps
+        graph_ms = time_loop(torch, stream, g.replay, 5) / (5 * reps)
+        out[f"{M}x{N}x{K}"] = {"eager_us": round(eager_ms * 1e3, 2), "graph_us": round(graph_ms * 1e3, 2)}
+        del g
+    return out
+
+
 def measure_rows(torch, tp, stream, peaks, flush_buf):
     """The path's other rows, each with its own roofline."""
     import numpy as np
@@ -365,6 +400,11 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         g()
     med, best = time_each_flushed(torch, stream, g, 50, flush_buf)
     rows["gemm_320x200x448_f32"] = {"unit": "us", "median_us": round(med * 1e3, 2), "min_us": round(best * 1e3, 2)}
+
+    # The same small GEMMs back to back: eager launches from Python against a
+    # CUDA graph of the same launches (no host cost per call; consecutive
+    # launches overlap their set-up through programmatic dependent launch).
+    rows["small_gemm_launch_latency"] = small_gemm_latency(torch, tp, stream)
 
     # 1 GiB TMA copy (input 1 GiB >> L2: back to back)
     rr, cc = 32768, 16384
