@@ -1,0 +1,117 @@
+"""Seeded random GEMMs and convolutions through the C ABI against the oracle,
+every output element checked. Shapes, pitches, base offsets (aligned or not:
+the plain-load producer and plain-store epilogue paths), output type and the
+launch options (atom, MMA N, ring depth, grid cap, raster group, tail, L2
+priorities) are drawn from one seeded generator, so a failure names a case
+that reruns exactly. Padding around C is a NaN sentinel that must survive."""
+import random
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import datagen  # noqa: E402
+import oracle  # noqa: E402
+import mbarrier_pipelined_tensor_gb300 as tp  # noqa: E402
+from gpu_util import check_against_oracle, dev_bf16, expect_ok, host_f64, new_out  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+N_GEMM = 40
+N_CONV = 24
+
+
+def _depths():
+    d = {}
+    for k in tp.tp_list_kernels():
+        if not (k["conv"] or k["ldg"] or k["splitk"]):
+            d.setdefault((k["atom"], k["tile_n"], k["out_f32"]), []).append(k["pipe_depth"])
+    return d
+
+
+def _gemm_case(i, depths):
+    rng = random.Random(1000 + i)
+    M = rng.choice([1, 3, 64, 128, 129, 200, 256, 257, 384, 500, rng.randint(1, 700)])
+    N = rng.choice([1, 5, 8, 64, 120, 128, 200, 256, 300, rng.randint(1, 700)])
+    K = rng.choice([1, 8, 16, 40, 64, 65, 128, 448, 1000, rng.randint(1, 1500)])
+    aligned = rng.random() < 0.7
+    lda = K + (rng.choice([0, 8, 16]) if aligned and K % 8 == 0 else rng.choice([0, 1, 3]))
+    ldb = K + (rng.choice([0, 8]) if aligned and K % 8 == 0 else rng.choice([0, 2]))
+    ldc = N + rng.choice([0, 3, 8])
+    offs = (0, 0, 0) if aligned else (rng.choice([0, 1, 4]), rng.choice([0, 3]), rng.choice([0, 1]))
+    out_f32 = rng.random() < 0.5
+    opts = {}
+    if rng.random() < 0.5:
+        opts["atom"] = rng.choice([1, 2])
+        opts["tile_n"] = rng.choice([128, 256])
+        ds = depths.get((opts["atom"], opts["tile_n"], int(out_f32)), [])
+        if ds and rng.random() < 0.5 and aligned:
+            opts["pipe_depth"] = rng.choice(ds)
+    if rng.random() < 0.3:
+        opts["max_ctas"] = rng.choice([2, 4, 6, 16])
+    if rng.random() < 0.3:
+        opts["group_m"] = rng.choice([1, 2, 3])
+    if rng.random() < 0.2:
+        opts["no_tail"] = 1
+    if rng.random() < 0.3:
+        opts["l2_hint"] = rng.randint(1, 6)
+    return M, N, K, lda, ldb, ldc, offs, out_f32, opts
+
+
+@pytest.mark.parametrize("i", range(N_GEMM))
+def test_fuzz_gemm(i):
+    M, N, K, lda, ldb, ldc, (oa, ob, oc), out_f32, opts = _gemm_case(i, _depths())
+    A, B = datagen.gemm_operands(M, N, K, seed=5000 + i, lda=lda, ldb=ldb)
+    a_all = dev_bf16(np.concatenate([np.zeros(oa, np.uint16), A.reshape(-1)]))
+    b_all = dev_bf16(np.concatenate([np.zeros(ob, np.uint16), B.reshape(-1)]))
+    c_all = new_out(1, M * ldc + oc + 7, out_f32).reshape(-1)
+    try:
+        tp.tp_gemm_bf16_ex(a_all[oa:], b_all[ob:], c_all[oc:], M, N, K, lda, ldb, ldc, out_f32=out_f32, **opts)
+    except tp.TPError as e:
+        # Explicit choices the library does not offer for this case (e.g. the
+        # plain-load producer exists only for the 1-SM atom at N = 128).
+        assert e.status == tp.TP_ERR_UNSUPPORTED and opts, (e, opts)
+        return
+    expect_ok()
+    full = host_f64(c_all)
+    assert np.all(np.isnan(full[:oc])) and np.all(np.isnan(full[oc + M * ldc:]))
+    got = full[oc:oc + M * ldc].reshape(M, ldc)
+    assert np.all(np.isnan(got[:, N:])), "wrote past N"
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    check_against_oracle(got[:, :N], ref, ab, out_f32, f"fuzz gemm {i}: {M}x{N}x{K} {opts}")
+
+
+def _conv_case(i):
+    rng = random.Random(2000 + i)
+    R, S = rng.choice([1, 3, 5, 2]), rng.choice([1, 3, 5, 2])
+    pad = rng.randint(0, 2)
+    st = rng.choice([1, 1, 2, 3])
+    H = rng.randint(max(1, R - 2 * pad), 24)
+    W = rng.randint(max(1, S - 2 * pad), 24)
+    Nb = rng.randint(1, 3)
+    C = rng.choice([8, 16, 64, 72, 128, 3, 20])
+    K = rng.choice([8, 64, 100, 128, 256, 264])
+    out_f32 = rng.random() < 0.5
+    opts = {}
+    if rng.random() < 0.4:
+        opts["atom"] = rng.choice([1, 2])
+    return Nb, H, W, C, K, R, S, st, pad, out_f32, opts
+
+
+@pytest.mark.parametrize("i", range(N_CONV))
+def test_fuzz_conv(i):
+    Nb, H, W, C, K, R, S, st, pad, out_f32, opts = _conv_case(i)
+    x, w = datagen.conv_operands(Nb, H, W, C, K, R, S, seed=7000 + i)
+    P, Q = oracle.conv_out_hw(H, W, R, S, st, pad)
+    y = new_out(Nb * P * Q, K, out_f32)
+    try:
+        tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, Nb, H, W, C, K, R, S, st, pad, out_f32=out_f32,
+                                   **opts)
+    except tp.TPError as e:
+        assert e.status == tp.TP_ERR_UNSUPPORTED and opts, (e, opts)
+        return
+    expect_ok()
+    ref, ab = oracle.conv(x, w, Nb, H, W, C, K, R, S, st, pad)
+    check_against_oracle(host_f64(y), ref, ab, out_f32,
+                         f"fuzz conv {i}: N{Nb} {H}x{W}x{C} -> {K} {R}x{S}/{st} pad {pad} {opts}")
