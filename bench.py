@@ -497,16 +497,25 @@ def reference_arm(args):
     A, B = datagen.gemm_operands(M, N, K, seed=1, dist="normal")
     import oracle
     per_step_rows = max(1, oracle.threads())  # one row of C per oracle thread
+    # Each step is the same bounded sample: per_step_rows rows of C over
+    # `ncols` columns spread across N, sized from one timed full-width step
+    # so that --steps of them take about 100 s of CPU work.
+    t0 = time.perf_counter()
+    oracle.gemm(A, B, M, N, K, K, K, rows=np.arange(per_step_rows))
+    t_full = time.perf_counter() - t0
+    budget_s = 100.0
+    ncols = N if args.steps * t_full <= budget_s else max(64, int(N * budget_s / (args.steps * t_full)) // 64 * 64)
+    cols = np.arange(ncols) * (N // ncols)
     for _ in range(max(0, args.warmup)):
-        oracle.gemm(A, B, M, N, K, K, K, rows=np.arange(1))
+        oracle.gemm(A, B, M, N, K, K, K, rows=np.arange(per_step_rows), cols=cols)
     t0 = time.perf_counter()
     for i in range(args.steps):
         rows = (np.arange(per_step_rows) * 1021 + i * 7) % M
-        oracle.gemm(A, B, M, N, K, K, K, rows=rows)
+        oracle.gemm(A, B, M, N, K, K, K, rows=rows, cols=cols)
     dt = time.perf_counter() - t0
-    flops = 2.0 * per_step_rows * N * K * args.steps
+    flops = 2.0 * per_step_rows * ncols * K * args.steps
     v = flops / dt / 1e12
-    sample = f"{per_step_rows} rows of C per step (all {N} columns, K={K})"
+    sample = f"{per_step_rows} rows x {ncols} of {N} columns of C per step (K={K})"
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
