@@ -67,3 +67,32 @@ def test_long_k_split(long_k):
     assert tp.tp_last_plan()["splits"] == 16
     got = host_f64(c.index_select(0, torch.from_numpy(g["rows"]).cuda()))
     check_against_oracle(got, g["ref"], g["ab"], True, "K = 2^20 split 16")
+
+
+def _pattern(rows, cols):
+    """rows x cols 16-bit patterns (any bits, NaN payloads included), made on
+    the device by torch: a copy's expected result is its own source."""
+    n = rows * cols
+    g = torch.arange(n, dtype=torch.int64, device="cuda")
+    return ((g * 2654435761 + (g >> 13)) & 0xFFFF).to(torch.int32).to(torch.int16).view(rows, cols)
+
+
+@pytest.mark.parametrize("force_vec", [False, True], ids=["tma", "vectorized"])
+def test_copy_beyond_2_31_elements(force_vec):
+    rows, cols = 131075, 16392                      # 2.149e9 elements, 4.3 GB each way
+    src = _pattern(rows, cols)
+    assert src.numel() > (1 << 31)
+    dst = torch.zeros_like(src)
+    tp.tp_tma_copy_2d_ex(src, dst, rows, cols, cols, force_vec=force_vec)
+    expect_ok()
+    assert torch.equal(src, dst)
+    del dst
+
+
+def test_transpose_beyond_2_31_elements():
+    rows, cols = 131075, 16392
+    src = _pattern(rows, cols)
+    dst = torch.empty((cols, rows), dtype=torch.int16, device="cuda")
+    tp.tp_tma_transpose_2d(src, dst, rows, cols, cols, rows)
+    expect_ok()
+    assert torch.equal(dst, src.t())

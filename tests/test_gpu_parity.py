@@ -433,3 +433,21 @@ def test_gemm_host_buffers_k0_and_errors():
     with pytest.raises(tp.TPError) as e:
         tp.tp_gemm_bf16_host(None, None, c_h, M, N, 4, 4, 4, N, None, None, dC, out_f32=True)
     assert e.value.status == tp.TP_ERR_INVALID_ARG
+
+
+def test_gemm_host_buffers_pageable():
+    # Pageable (not page-locked) host memory: the copies are staged by the
+    # driver and block the host, with the same result.
+    M, N, K = 200, 136, 256
+    A, B = datagen.gemm_operands(M, N, K, seed=58)
+    a_h, b_h = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    c_h = np.zeros((M, N), dtype=np.float32)
+    dA = torch.empty(M * K, dtype=torch.int16, device="cuda")
+    dB = torch.empty(N * K, dtype=torch.int16, device="cuda")
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    tp.tp_gemm_bf16_host(a_h.ctypes.data, b_h.ctypes.data, c_h.ctypes.data, M, N, K, K, K, N, dA, dB, dC,
+                         out_f32=True)
+    torch.cuda.synchronize()
+    expect_ok()
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(c_h.astype(np.float64), ref, ab, True, "pageable host buffers")
