@@ -91,7 +91,10 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   pipe_depth: PIPE_DEPTH, stages in the ring (2..9).
  *   tile_n:     MMA N (128 or 256).
  *   group_m:    tile raster: group_m M-tiles share one sweep over N.
- *   max_ctas:   cap on the persistent grid (0 = one CTA per SM).
+ *   max_ctas:   cap on the persistent grid (0 = one CTA per SM). A cap at
+ *               or above the tile count (CTAs = tiles x atom) launches one
+ *               work unit per cluster, i.e. a non-persistent grid that the
+ *               hardware schedules in waves.
  *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
  *               1 none, 2 A evict-last / B evict-first, 3 A evict-last,
  *               4 B evict-first, 5 A evict-first / B evict-last, 6 B
