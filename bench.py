@@ -484,6 +484,51 @@ def cpu_baseline(M, N, K, A, B, target_s=12.0):
             "seconds": round(dt, 2)}
 
 
+def row_oracle_timings(rows):
+    """The oracle timed per row: the small configurations in full, the
+    others on a sample of C's rows (conv: output pixels), reported as sampled
+    MAC/s and the full problem's time extrapolated from it (labelled)."""
+    import numpy as np
+    import datagen
+    import oracle
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return max(time.perf_counter() - t0, 1e-6)
+
+    def entry(macs, full_macs, dt, sample):
+        e = {"sample": sample, "macs": int(macs), "seconds": round(dt, 4),
+             "gmac_per_s": round(macs / dt / 1e9, 3), "cores": oracle.threads()}
+        if macs < full_macs:
+            e["extrapolated_full_s"] = round(full_macs / (macs / dt), 2)
+        return e
+
+    thr = max(1, oracle.threads())
+    out = {}
+    if "gemm_320x200x448_f32" in rows:
+        A, B = datagen.gemm_operands(320, 200, 448, seed=0)
+        dt = timed(lambda: oracle.gemm(A, B, 320, 200, 448, 448, 448))
+        out["gemm_320x200x448_f32"] = entry(320 * 200 * 448, 320 * 200 * 448, dt, "full")
+    for (M, N, K), (A, B) in zip(datagen.SKINNY_SHAPES, datagen.skinny_operands()):
+        key = f"{M}x{N}x{K}"
+        full = M * N * K
+        if full <= 2_000_000_000:
+            dt = timed(lambda: oracle.gemm(A, B, M, N, K, K, K))
+            out[key] = entry(full, full, dt, "full")
+        else:
+            r = np.linspace(0, M - 1, min(M, thr * 2)).astype(np.int64)
+            dt = timed(lambda: oracle.gemm(A, B, M, N, K, K, K, rows=r))
+            out[key] = entry(r.size * N * K, full, dt, f"{r.size} of {M} rows of C")
+    Nb, H, W, C, K, R, S = 32, 56, 56, 256, 256, 3, 3
+    x, w = datagen.conv_operands(Nb, H, W, C, K, R, S, seed=2)
+    pix = np.linspace(0, Nb * H * W - 1, thr * 16).astype(np.int64)
+    dt = timed(lambda: oracle.conv(x, w, Nb, H, W, C, K, R, S, 1, 1, pixels=pix))
+    out["conv_32x56x56x256_3x3"] = entry(pix.size * K * R * S * C, Nb * H * W * K * R * S * C, dt,
+                                         f"{pix.size} of {Nb * H * W} output pixels")
+    return out
+
+
 # ----------------------------------------------------------------- arms ---
 
 def reference_arm(args):
@@ -664,6 +709,12 @@ def tp_arm(args):
         sweep = run_sweep(torch, tp, stream, a, b, c, M, N, K, peaks)
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(M, N, K, A, B)
+        if rows:
+            for key, e in row_oracle_timings(rows).items():
+                if key in rows:
+                    rows[key]["cpu_oracle"] = e
+                elif key in rows.get("skinny_gemm_set", {}):
+                    rows["skinny_gemm_set"][key]["cpu_oracle"] = e
 
     if rank == 0:
         kname = "mainloop_kernel"
