@@ -90,19 +90,24 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               stages: "two-free-pipeline-stages", stage budget table).
  *   pipe_depth: PIPE_DEPTH, stages in the ring (2..9).
  *   tile_n:     MMA N (128 or 256).
- *   group_m:    tile raster: group_m M-tiles share one sweep over N.
+ *   group_m:    tile raster: group_m M-tiles share one sweep over N
+ *               (0 = 2048 rows of A per group: 16 tiles of the 1-SM atom,
+ *               8 pair tiles of the 2-SM atom).
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM). A cap at
  *               or above the tile count (CTAs = tiles x atom) launches one
  *               work unit per cluster, i.e. a non-persistent grid that the
  *               hardware schedules in waves.
  *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
- *               1 none, 2 A evict-last / B evict-first, 3 A evict-last,
- *               4 B evict-first, 5 A evict-first / B evict-last, 6 B
- *               evict-last. "Choose" (GEMM only; the convolution keeps 1)
- *               picks 2 when at most two tile rows read B and A is small
- *               (<= 16 MB, under a quarter of B): B then streams through L2
- *               once while A, read by every tile, stays. It picks 5 in the
- *               mirrored case, else 1.
+ *               1 none (no cache-hint policy), 2 A evict-last / B
+ *               evict-first, 3 A evict-last, 4 B evict-first, 5 A
+ *               evict-first / B evict-last, 6 B evict-last, 7 an explicit
+ *               evict_normal policy on both (not the same as 1: on GB300
+ *               the unhinted loads measured faster for every variant).
+ *               "Choose" (GEMM only; the convolution keeps 1) picks 2 when
+ *               at most two tile rows read B and A is small (<= 16 MB,
+ *               under a quarter of B): B then streams through L2 once while
+ *               A, read by every tile, stays. It picks 5 in the mirrored
+ *               case, else 1.
  *   no_tail:    1 keeps whole tiles in the last wave (the 2-SM, N = 256
  *               variant otherwise runs a partial last wave as half-width
  *               tiles).

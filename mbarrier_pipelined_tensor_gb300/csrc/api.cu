@@ -307,9 +307,12 @@ int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom)
     return c < 1 ? 1 : c;
 }
 
-int group_m_for(const tp_gemm_opts* o, int64_t m_tiles)
+// Tile raster: group_m M-tiles share one sweep over N. By default a group
+// spans 2048 rows of A (16 tiles of the 1-SM atom, 8 pair tiles of the 2-SM
+// atom): measured best for both at 6144^3 and 8192^3 on GB300.
+int group_m_for(const tp_gemm_opts* o, int64_t m_tiles, int atom)
 {
-    int g = o && o->group_m > 0 ? o->group_m : 8;
+    int g = o && o->group_m > 0 ? o->group_m : 2048 / (128 * (atom > 0 ? atom : 1));
     if (g > m_tiles) g = static_cast<int>(m_tiles);
     return g < 1 ? 1 : g;
 }
@@ -331,6 +334,8 @@ int l2_mode_for(const tp_gemm_opts* o, int64_t m_tiles, int64_t n_tiles, double 
     return 1;
 }
 
+// Per-operand load policies (GemmParams::l2_a / l2_b): 0 no policy, 1 evict
+// first, 2 evict last, 3 an explicit evict_normal policy.
 void l2_hints_for(int mode, int* a, int* b)
 {
     *a = 0;
@@ -341,7 +346,8 @@ void l2_hints_for(int mode, int* a, int* b)
     case 4: *b = 1; break;
     case 5: *a = 1; *b = 2; break;
     case 6: *b = 2; break;
-    default: break;  // 1: normal priority
+    case 7: *a = 3; *b = 3; break;
+    default: break;  // 1: normal priority, no policy
     }
 }
 
@@ -369,7 +375,7 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
     // does not decide it: a C that TMA cannot store is written with plain
     // stores by the epilogue.
     const int ldg = (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16) ? 1 : 0;
-    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 6)) return TP_ERR_INVALID_ARG;
+    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 7)) return TP_ERR_INVALID_ARG;
     const int st = plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl);
     if (st == TP_OK)
         pl->l2_hint = l2_mode_for(opts, pl->m_tiles, pl->n_tiles, 2.0 * static_cast<double>(M) * static_cast<double>(K),
@@ -575,7 +581,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.kb_per_split = use_splitk ? kps : p.k_blocks;
     if (!use_splitk && !(opts && opts->no_tail))
         set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
-    p.group_m = group_m_for(opts, pl.m_tiles);
+    p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
@@ -677,7 +683,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     // TMA; otherwise the epilogue writes y with plain stores.
     const bool y_tma = aligned16(y) && (K * eb_out) % 16 == 0;
     const int64_t cblocks = cdiv(C, 64);
-    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 6)) return TP_ERR_INVALID_ARG;
+    if (opts && (opts->l2_hint < 0 || opts->l2_hint > 7)) return TP_ERR_INVALID_ARG;
     st = plan_mainloop(M, K, R * S * cblocks, out_f32, 1, ldg, opts, dev->sm_count, &pl);
     if (st) return st;
     const int cg = pl.atom;
@@ -740,7 +746,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
     if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
-    p.group_m = group_m_for(opts, pl.m_tiles);
+    p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     pl.l2_hint = l2_mode_for(opts, pl.m_tiles, pl.n_tiles, 0.0, 0.0, false);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.conv_P = static_cast<int>(P);

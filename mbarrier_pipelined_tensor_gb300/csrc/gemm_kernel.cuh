@@ -38,6 +38,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace tp {
@@ -308,72 +310,111 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp == 0) {
         // --------------------------------------------------- producer ---
         if (elect_one()) {
-            const uint64_t pol_a = make_l2_policy(p.l2_a);
-            const uint64_t pol_b = make_l2_policy(p.l2_b);
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
             bool ok = true;
             unsigned long long t_wait = 0;
             const uint64_t t_start = p.trace ? globaltimer_ns() : 0;
-            for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
-                const Unit w = unit_of(u, num_tiles, p);
-                int mt, nt;
-                tile_coords(w.tile, p, mt, nt);
-                const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
-                // A half-width unit (2-SM only) needs BN/4 rows of B per CTA,
-                // starting at its half; the B box (BN/2 rows) loads them first.
-                const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
-                                             : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
-                int img = 0, base_h = 0, base_w = 0;
-                if constexpr (CONV) {
-                    const int pq = p.conv_P * p.conv_Q;
-                    img = m_row / pq;
-                    const int rem = m_row - img * pq;
-                    const int pp = rem / p.conv_Q;
-                    const int qq = rem - pp * p.conv_Q;
-                    base_h = pp * p.conv_stride - p.conv_pad;
-                    base_w = qq * p.conv_stride - p.conv_pad;
-                }
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!timed_wait<CL>(p, empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY, t_wait)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = CL ? mapa_shared(full_bar(s), 0) : full_bar(s);
-                    if (leader && !(p.withhold_first_arrival && issued == 0))
-                        mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
-                    const uint32_t dA = sA + s * Cfg::A_BYTES;
-                    const uint32_t dB = sB + s * Cfg::B_BYTES;
+            // The k-loop is one thread's critical path (a stage every ~256
+            // cycles at MMA N = 128), so it is kept lean: the cache-hint
+            // choice is made once, by instantiating the loop for it; the
+            // leader's full barriers are addressed from one mapa; the conv's
+            // (tap, channel block) coordinates step instead of dividing.
+            auto run = [&](auto hint_a_t, auto hint_b_t) {
+                constexpr bool HA = decltype(hint_a_t)::value;
+                constexpr bool HB = decltype(hint_b_t)::value;
+                const uint64_t pol_a = HA ? make_l2_policy(p.l2_a) : 0;
+                const uint64_t pol_b = HB ? make_l2_policy(p.l2_b) : 0;
+                const uint32_t fb0 = CL ? mapa_shared(full_bar(0), 0) : full_bar(0);
+                bool arrive = !p.withhold_first_arrival;  // the self test withholds the very first arrival
+                for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                    const Unit w = unit_of(u, num_tiles, p);
+                    int mt, nt;
+                    tile_coords(w.tile, p, mt, nt);
+                    const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
+                    // A half-width unit (2-SM only) needs BN/4 rows of B per CTA,
+                    // starting at its half; the B box (BN/2 rows) loads them first.
+                    const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
+                                                 : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
+                    int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
                     if constexpr (CONV) {
-                        const int rs = kb / p.conv_cblocks;
-                        const int c0 = (kb - rs * p.conv_cblocks) * Cfg::BK;
-                        const int r = rs / p.conv_S;
-                        const int sx = rs - r * p.conv_S;
-                        if constexpr (CL) {
-                            tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img,
-                                                    static_cast<uint16_t>(sx), static_cast<uint16_t>(r), pol_a);
-                            tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row, pol_b);
-                        } else {
-                            tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img,
-                                               static_cast<uint16_t>(sx), static_cast<uint16_t>(r), pol_a);
-                            tma_load_3d(dB, &mapB, fb, c0, rs, n_row, pol_b);
-                        }
-                    } else {
-                        if constexpr (CL) {
-                            tma_load_2d_pair(dA, &mapA, fb, kb * Cfg::BK, m_row, pol_a);
-                            tma_load_2d_pair(dB, &mapB, fb, kb * Cfg::BK, n_row, pol_b);
-                        } else {
-                            tma_load_2d(dA, &mapA, fb, kb * Cfg::BK, m_row, pol_a);
-                            tma_load_2d(dB, &mapB, fb, kb * Cfg::BK, n_row, pol_b);
-                        }
+                        const int pq = p.conv_P * p.conv_Q;
+                        img = m_row / pq;
+                        const int rem = m_row - img * pq;
+                        const int pp = rem / p.conv_Q;
+                        const int qq = rem - pp * p.conv_Q;
+                        base_h = pp * p.conv_stride - p.conv_pad;
+                        base_w = qq * p.conv_stride - p.conv_pad;
+                        rs = w.kb0 / p.conv_cblocks;
+                        cb = w.kb0 - rs * p.conv_cblocks;
+                        r = rs / p.conv_S;
+                        sx = rs - r * p.conv_S;
                     }
-                    ++issued;
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                        if (!timed_wait<CL>(p, empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY, t_wait)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb = fb0 + 8u * static_cast<uint32_t>(s);
+                        if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
+                        arrive = true;
+                        const uint32_t dA = sA + s * Cfg::A_BYTES;
+                        const uint32_t dB = sB + s * Cfg::B_BYTES;
+                        if constexpr (CONV) {
+                            const int c0 = cb * Cfg::BK;
+                            const uint16_t ow = static_cast<uint16_t>(sx), oh = static_cast<uint16_t>(r);
+                            if constexpr (CL) {
+                                if constexpr (HA) tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh, pol_a);
+                                else tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh);
+                                if constexpr (HB) tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row, pol_b);
+                                else tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row);
+                            } else {
+                                if constexpr (HA) tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh, pol_a);
+                                else tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh);
+                                if constexpr (HB) tma_load_3d(dB, &mapB, fb, c0, rs, n_row, pol_b);
+                                else tma_load_3d(dB, &mapB, fb, c0, rs, n_row);
+                            }
+                            if (++cb == p.conv_cblocks) {
+                                cb = 0;
+                                ++rs;
+                                if (++sx == p.conv_S) {
+                                    sx = 0;
+                                    ++r;
+                                }
+                            }
+                        } else {
+                            const int kx = kb * Cfg::BK;
+                            if constexpr (CL) {
+                                if constexpr (HA) tma_load_2d_pair(dA, &mapA, fb, kx, m_row, pol_a);
+                                else tma_load_2d_pair(dA, &mapA, fb, kx, m_row);
+                                if constexpr (HB) tma_load_2d_pair(dB, &mapB, fb, kx, n_row, pol_b);
+                                else tma_load_2d_pair(dB, &mapB, fb, kx, n_row);
+                            } else {
+                                if constexpr (HA) tma_load_2d(dA, &mapA, fb, kx, m_row, pol_a);
+                                else tma_load_2d(dA, &mapA, fb, kx, m_row);
+                                if constexpr (HB) tma_load_2d(dB, &mapB, fb, kx, n_row, pol_b);
+                                else tma_load_2d(dB, &mapB, fb, kx, n_row);
+                            }
+                        }
+                        ++issued;
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
                     }
                 }
+            };
+            // A load carries a cache-hint policy only when its operand's
+            // priority asks for one (l2_a / l2_b != 0; 3 = explicit normal).
+            using T = std::true_type;
+            using F = std::false_type;
+            if (p.l2_a != 0) {
+                if (p.l2_b != 0) run(T{}, T{});
+                else run(T{}, F{});
+            } else {
+                if (p.l2_b != 0) run(F{}, T{});
+                else run(F{}, F{});
             }
             if (p.trace) {
                 trace_add(p, TRACE_PRODUCER_SPAN, globaltimer_ns() - t_start);

@@ -253,4 +253,5 @@ def test_l2_priority_choice():
     assert mode(128, 256, 64) == 1          # B not much bigger than A
     assert mode(128, 8192, 16384, l2_hint=1) == 1
     assert mode(8192, 8192, 8192, l2_hint=4) == 4
-    assert plan(128, 128, 128, l2_hint=7)[0] == tp.TP_ERR_INVALID_ARG
+    assert mode(8192, 8192, 8192, l2_hint=7) == 7   # explicit evict_normal policy
+    assert plan(128, 128, 128, l2_hint=8)[0] == tp.TP_ERR_INVALID_ARG
