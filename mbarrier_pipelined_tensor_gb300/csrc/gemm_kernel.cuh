@@ -450,6 +450,13 @@ __global__ void __launch_bounds__(192, 1)
                 bool ok = true;
                 unsigned long long t_full = 0, t_acc = 0;
                 const uint64_t t_start = p.trace ? globaltimer_ns() : 0;
+                // Like the producer's, this loop is a single thread's critical
+                // path. The descriptors of stage s and K step k differ from
+                // those of stage 0 only in the start-address field (address /
+                // 16, below 2^14 in the CTA's shared window, so adding to it
+                // never carries): they are formed once and advanced by adds.
+                const uint64_t dA0 = umma_desc_sw128_kmajor(sA);
+                const uint64_t dB0 = umma_desc_sw128_kmajor(sB);
                 for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++lt) {
                     const Unit w = unit_of(u, num_tiles, p);
                     const int b = lt & 1;
@@ -457,20 +464,21 @@ __global__ void __launch_bounds__(192, 1)
                     if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
                     tcgen05_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                    const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
+                    uint32_t accumulate = 0;  // the unit's first MMA overwrites the accumulator
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         if (!timed_wait<CL>(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
                             ok = false;
                             break;
                         }
                         tcgen05_fence_after();
-                        const uint32_t aS = sA + s * Cfg::A_BYTES;
-                        const uint32_t bS = sB + s * Cfg::B_BYTES;
+                        const uint64_t da = dA0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
+                        const uint64_t db = dB0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
-                            const uint64_t da = umma_desc_sw128_kmajor(aS + k * 32);
-                            const uint64_t db = umma_desc_sw128_kmajor(bS + k * 32);
-                            umma_bf16<CG>(d_tmem, da, db, w.half < 0 ? IDESC : IDESC_HALF,
-                                          (kb != w.kb0 || k != 0) ? 1u : 0u);
+                            // +32 bytes per K step of 16 inside the swizzle atom
+                            umma_bf16<CG>(d_tmem, da + 2 * k, db + 2 * k, idesc, accumulate);
+                            accumulate = 1;
                         }
                         if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
                         else umma_commit(empty_bar(s));
