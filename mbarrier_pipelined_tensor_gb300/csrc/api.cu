@@ -175,7 +175,7 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
     };
     // Efficiency relative to the 2-SM / N = 256 variant: the PIPE_DEPTH
     // sweep at 8192^3 on GB300 (deepest ring of each variant).
-    static const Cand kCands[] = {{2, 256, 1.00}, {1, 256, 0.86}, {2, 128, 0.84}, {1, 128, 0.76}};
+    static const Cand kCands[] = {{2, 256, 1.00}, {1, 256, 0.86}, {2, 128, 0.89}, {1, 128, 0.75}};
     double best = 0;
     Cand pick = kCands[0];
     bool have = false;
