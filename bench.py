@@ -442,11 +442,67 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
     return rows
 
 
+def library_comparison(torch, stream, flush_buf, headline_step):
+    """The same workloads through PyTorch's vendor-library kernels (cuBLAS for
+    the GEMMs, cuDNN for the conv, PyTorch's own copy kernels), timed the same
+    way as the rows above. Context only: none of it is on the library's path."""
+    import numpy as np
+    import datagen
+    out = {"note": "torch.mm (cuBLAS), torch conv2d channels_last (cuDNN, benchmark mode), torch copy_; "
+                   "same timing as the rows: flushed medians for GEMMs/conv, back-to-back for 1 GiB copies"}
+    with torch.cuda.stream(stream):
+        N, H, W, C, K, R, S = 32, 56, 56, 256, 256, 3, 3
+        x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=2)
+        # NHWC / KRSC bytes viewed as channels_last NCHW / KCRS tensors
+        xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16).view(N, H, W, C).permute(0, 3, 1, 2)
+        wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16).view(K, R, S, C).permute(0, 3, 1, 2)
+        flops = 2.0 * N * H * W * K * R * S * C
+        prev = torch.backends.cudnn.benchmark
+        torch.backends.cudnn.benchmark = True
+        try:
+            cv = lambda: torch.nn.functional.conv2d(xd, wd, padding=1)  # noqa: E731
+            for _ in range(5):
+                cv()
+            med, _ = time_each_flushed(torch, stream, cv, 20, flush_buf)
+        finally:
+            torch.backends.cudnn.benchmark = prev
+        out["conv_32x56x56x256_3x3"] = {"us": round(med * 1e3, 2), "tflops": round(flops / (med * 1e-3) / 1e12, 1)}
+        del xd, wd
+        for (Ms, Ns, Ks) in ((8192, 8192, 8192), (128, 8192, 16384), (4096, 4096, 512), (1000, 1000, 1000),
+                             (320, 200, 448)):
+            a = torch.randn(Ms, Ks, device="cuda").bfloat16()
+            b = torch.randn(Ns, Ks, device="cuda").bfloat16()
+            mm = lambda: torch.mm(a, b.t())  # noqa: E731
+            for _ in range(5):
+                mm()
+            med, _ = time_each_flushed(torch, stream, mm, 20, flush_buf)
+            f = 2.0 * Ms * Ns * Ks
+            out[f"gemm_{Ms}x{Ns}x{Ks}"] = {"us": round(med * 1e3, 2), "tflops": round(f / (med * 1e-3) / 1e12, 1)}
+            del a, b
+        # this library's headline launch under the same flushed timing
+        med, _ = time_each_flushed(torch, stream, headline_step, 20, flush_buf)
+        out["gemm_8192x8192x8192_this_library"] = {"us": round(med * 1e3, 2),
+                                                   "tflops": round(2.0 * 8192 ** 3 / (med * 1e-3) / 1e12, 1)}
+        rr, cc = 32768, 16384
+        src = torch.empty((rr, cc), dtype=torch.int16, device="cuda").random_(-32768, 32767)
+        moved = 2.0 * rr * cc * 2
+        for name, dst, fn in (("copy_1GiB", torch.empty_like(src), lambda d: d.copy_(src)),
+                              ("transpose_1GiB", torch.empty((cc, rr), dtype=torch.int16, device="cuda"),
+                               lambda d: d.copy_(src.t()))):
+            for _ in range(3):
+                fn(dst)
+            ms = time_loop(torch, stream, lambda: fn(dst), 20) / 20
+            out[name] = {"gbs": round(moved / (ms * 1e-3) / 1e9, 1), "ms": round(ms, 4)}
+            del dst
+        del src
+    return out
+
+
 def run_sweep(torch, tp, stream, a, b, c, M, N, K, peaks):
     out = []
     s = stream.cuda_stream
-    for atom, tile_n, depths in ((1, 128, range(2, 8)), (2, 128, range(2, 10)), (1, 256, range(2, 6)),
-                                 (2, 256, range(2, 8))):
+    for atom, tile_n, depths in ((1, 64, range(2, 10)), (1, 128, range(2, 8)), (2, 128, range(2, 10)),
+                                 (1, 256, range(2, 6)), (2, 256, range(2, 8))):
         for d in depths:
             st, byts = tp.tp_query_smem_bytes(atom, d, tile_n)
             row = {"atom": atom, "tile_n": tile_n, "pipe_depth": d, "smem_bytes": byts}
@@ -704,6 +760,7 @@ def tp_arm(args):
     if rank == 0 and not args.no_rows:
         flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
         rows = measure_rows(torch, tp, stream, peaks, flush_buf)
+        rows["library_comparison"] = library_comparison(torch, stream, flush_buf, step)
         del flush_buf
     if rank == 0 and args.sweep:
         sweep = run_sweep(torch, tp, stream, a, b, c, M, N, K, peaks)

@@ -89,7 +89,12 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               CTA holds half of B, which frees shared memory for more
  *               stages: "two-free-pipeline-stages", stage budget table).
  *   pipe_depth: PIPE_DEPTH, stages in the ring (2..9).
- *   tile_n:     MMA N (128 or 256).
+ *   tile_n:     MMA N: 64 (1-SM atom only; 128 x 64 tiles with up to 8
+ *               stages, for problems whose wider tiles would leave most SMs
+ *               idle), 128 or 256. "Choose" estimates each compiled
+ *               variant's time from its waves of tiles, K blocks and measured
+ *               throughput; the split-K entry points choose among N >= 128
+ *               only.
  *   group_m:    tile raster: group_m M-tiles share one sweep over N
  *               (0 = 2048 rows of A per group: 16 tiles of the 1-SM atom,
  *               8 pair tiles of the 2-SM atom).

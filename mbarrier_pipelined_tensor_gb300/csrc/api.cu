@@ -22,6 +22,7 @@ const KernelEntry* table_mainloop_cg2(int* n);
 const KernelEntry* table_mainloop_conv(int* n);
 const KernelEntry* table_mainloop_fallback(int* n);
 const KernelEntry* table_mainloop_splitk(int* n);
+const KernelEntry* table_mainloop_n64(int* n);
 cudaError_t launch_splitk_reduce(const float* ws, void* C, int M, int N, int64_t ldw, int64_t ldc, int splits,
                                  int out_f32, int sm_count, cudaStream_t st);
 cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensorMap& d, const CopyParams& p,
@@ -111,7 +112,7 @@ int64_t splitk_ldw(int64_t N) { return (N + 3) / 4 * 4; }
 
 // ------------------------------------------------------ variant table ---
 
-constexpr int kTables = 5;
+constexpr int kTables = 6;
 
 struct Tables {
     const KernelEntry* t[kTables];
@@ -127,6 +128,7 @@ const Tables& tables()
         x.t[2] = table_mainloop_conv(&x.n[2]);
         x.t[3] = table_mainloop_fallback(&x.n[3]);
         x.t[4] = table_mainloop_splitk(&x.n[4]);
+        x.t[5] = table_mainloop_n64(&x.n[5]);
         return x;
     }();
     return tb;
@@ -166,8 +168,17 @@ int deepest_fitting(int atom, int tile_n)
 // output tiles over the persistent clusters and eff is the variant's
 // measured throughput on a large square GEMM relative to the best one
 // (2-SM, N = 256 at its deepest ring). A fixed field (*atom or *tile_n
-// nonzero) restricts the candidates.
-void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* atom, int* tile_n)
+// nonzero) restricts the candidates, and so does the kernel table: only
+// variants built for this output type and operand form (GEMM or conv) at
+// their deepest ring compete. (An explicit ring depth is checked after the
+// choice, against the shared-memory budget and the table.) For a split-K
+// call the N = 64 tile is left out: there the K slices already spread a
+// short tile row over the SMs, and a wider tile keeps more of B in flight
+// per CTA and re-reads A less (128 x 8192 x 16384 on GB300: N = 128 in 2
+// slices 59.7 us, N = 256 in 4 slices 58.8 us, N = 64 unsplit 61.9 us).
+// Returns false when no variant qualifies.
+bool choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int out_f32, int conv, int splitk,
+                    int* atom, int* tile_n)
 {
     struct Cand {
         int atom, tile_n;
@@ -175,12 +186,15 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
     };
     // Efficiency relative to the 2-SM / N = 256 variant: the PIPE_DEPTH
     // sweep at 8192^3 on GB300 (deepest ring of each variant).
-    static const Cand kCands[] = {{2, 256, 1.00}, {1, 256, 0.86}, {2, 128, 0.89}, {1, 128, 0.75}};
+    static const Cand kCands[] = {{2, 256, 1.00}, {1, 256, 0.86}, {2, 128, 0.89}, {1, 128, 0.75}, {1, 64, 0.54}};
     double best = 0;
     Cand pick = kCands[0];
     bool have = false;
     for (const Cand& c : kCands) {
         if ((*atom && c.atom != *atom) || (*tile_n && c.tile_n != *tile_n)) continue;
+        if (splitk && c.tile_n == 64) continue;
+        if (!find_kernel(KernelKey{c.atom, c.tile_n, deepest_fitting(c.atom, c.tile_n), out_f32, conv, 0, 0}))
+            continue;
         const int64_t tiles = cdiv(M, 128 * c.atom) * cdiv(N, c.tile_n);
         const int64_t clusters = std::max<int64_t>(1, sm_count / c.atom);
         double waves = static_cast<double>(cdiv(tiles, clusters));
@@ -195,7 +209,7 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
         // Short K: a narrow tile's fixed per-tile cost (ring fill, epilogue)
         // is a larger share of its work (4096 x 4096 x 512: N = 128 tiles
         // measured 27 us against 23 us for N = 256).
-        if (k_blocks <= 16 && c.tile_n == 128) cost *= 1.25;
+        if (k_blocks <= 16 && c.tile_n <= 128) cost *= 1.25;
         // A cluster launch and its pair barriers cost about 2 us more per
         // call than the 1-SM atom (a one-tile GEMM: 10.9 against 8.9 us).
         if (c.atom == 2) cost += 2000.0;
@@ -207,23 +221,26 @@ void choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int* a
     }
     *atom = pick.atom;
     *tile_n = pick.tile_n;
+    return have;
 }
 
 // Variant and launch shape for a GEMM view M x N x K (k_blocks given).
 int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv, int ldg, const tp_gemm_opts* o,
-                  int sm_count, tp_plan* pl)
+                  int sm_count, tp_plan* pl, int splitk = 0)
 {
     int atom = o && o->atom ? o->atom : 0;
     int tile_n = o && o->tile_n ? o->tile_n : 0;
     if (atom != 0 && atom != 1 && atom != 2) return TP_ERR_INVALID_ARG;
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256) return TP_ERR_INVALID_ARG;
+    if (tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256) return TP_ERR_INVALID_ARG;
     if (ldg) {
         // The plain-load producer exists for the 1-SM atom at N = 128 only.
         if ((atom && atom != 1) || (tile_n && tile_n != 128)) return TP_ERR_UNSUPPORTED;
         atom = 1;
         tile_n = 128;
     }
-    if (atom == 0 || tile_n == 0) choose_variant(M, N, k_blocks, sm_count, &atom, &tile_n);
+    if ((atom == 0 || tile_n == 0) &&
+        !choose_variant(M, N, k_blocks, sm_count, out_f32, conv, splitk, &atom, &tile_n))
+        return TP_ERR_UNSUPPORTED;
     int depth = o && o->pipe_depth ? o->pipe_depth : deepest_fitting(atom, tile_n);
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
     const int64_t smem = mainloop_smem(atom, depth, tile_n);
@@ -354,7 +371,8 @@ void l2_hints_for(int mode, int* a, int* b)
 }
 
 int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                   int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* pl)
+                   int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* pl,
+                   int splitk = 0)
 {
     std::memset(pl, 0, sizeof(*pl));
     if (M < 0 || N < 0 || K < 0) return TP_ERR_INVALID_ARG;
@@ -378,7 +396,7 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
     // stores by the epilogue.
     const int ldg = (!aligned16(A) || !aligned16(B) || (lda * 2) % 16 || (ldb * 2) % 16) ? 1 : 0;
     if (opts && (opts->l2_hint < 0 || opts->l2_hint > 7)) return TP_ERR_INVALID_ARG;
-    const int st = plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl);
+    const int st = plan_mainloop(M, N, cdiv(K, 64), out_f32, 0, ldg, opts, sm_count, pl, splitk);
     if (st == TP_OK)
         pl->l2_hint = l2_mode_for(opts, pl->m_tiles, pl->n_tiles, 2.0 * static_cast<double>(M) * static_cast<double>(K),
                                   2.0 * static_cast<double>(N) * static_cast<double>(K), true);
@@ -431,7 +449,7 @@ int tp_last_plan(tp_plan* plan)
 int tp_query_smem_bytes(int atom, int pipe_depth, int tile_n, int out_f32, int64_t* bytes)
 {
     (void)out_f32;  // the staging buffers are 128-byte rows for either output type
-    if ((atom != 1 && atom != 2) || (tile_n != 128 && tile_n != 256) || pipe_depth < 1 || !bytes)
+    if ((atom != 1 && atom != 2) || (tile_n != 64 && tile_n != 128 && tile_n != 256) || pipe_depth < 1 || !bytes)
         return TP_ERR_INVALID_ARG;
     *bytes = mainloop_smem(atom, pipe_depth, tile_n);
     return *bytes <= kMaxSmemPerCta ? TP_OK : TP_ERR_SMEM_BUDGET;
@@ -498,7 +516,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
         local.atom = 1;
         opts = &local;
     }
-    st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, dev->sm_count, &pl);
+    st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32, opts, dev->sm_count, &pl, splitk);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pl.path == TP_PATH_ZERO_FILL) {

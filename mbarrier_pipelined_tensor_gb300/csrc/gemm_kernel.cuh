@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(192, 1)
                     // starting at its half; the B box (BN/2 rows) loads them first.
                     const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
                                                  : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
-                    int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
+                    [[maybe_unused]] int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
                     if constexpr (CONV) {
                         const int pq = p.conv_P * p.conv_Q;
                         img = m_row / pq;

@@ -40,7 +40,7 @@ def test_splitk_skinny(splits, out_f32):
     check_against_oracle(got, ref, ab, out_f32, f"split-K {splits}")
 
 
-@pytest.mark.parametrize("atom,tile_n", [(1, 128), (1, 256), (2, 128), (2, 256)])
+@pytest.mark.parametrize("atom,tile_n", [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)])
 def test_splitk_every_variant_ragged(atom, tile_n):
     M, N, K = 300, 201, 1001
     lda = ldb = 1008

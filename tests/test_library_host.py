@@ -90,6 +90,9 @@ def test_library_budget_reproduces_page_depths():
 def test_query_rejects_impossible():
     assert tp.tp_query_smem_bytes(3, 4, 128)[0] == tp.TP_ERR_INVALID_ARG
     assert tp.tp_query_smem_bytes(1, 4, 96)[0] == tp.TP_ERR_INVALID_ARG
+    # 1-SM, N = 64: stages of 16 KiB A + 8 KiB B; 8 fit, 9 do not.
+    assert tp.tp_query_smem_bytes(1, 8, 64) == (tp.TP_OK, 230656)
+    assert tp.tp_query_smem_bytes(1, 9, 64)[0] == tp.TP_ERR_SMEM_BUDGET
 
 
 def test_compiled_variants_match_budget():
@@ -101,6 +104,15 @@ def test_compiled_variants_match_budget():
     sweep = {(k["atom"], k["pipe_depth"]) for k in ks if k["tile_n"] == 128 and not k["conv"] and not k["out_f32"]}
     assert {(1, d) for d in range(2, 7)} <= sweep
     assert {(2, d) for d in range(2, 9)} <= sweep
+    n64 = {k["pipe_depth"] for k in ks if k["tile_n"] == 64 and not k["conv"] and not k["out_f32"]}
+    assert set(range(2, 9)) <= n64
+    # Every variant the planner may pick by itself has all four output forms
+    # (bf16 / fp32 GEMM, bf16 / fp32 conv) and split-K at its deepest ring.
+    have = {(k["atom"], k["tile_n"], k["pipe_depth"], k["out_f32"], k["conv"], k["splitk"]) for k in ks
+            if not k["ldg"]}
+    for atom, tile_n, d in ((2, 256, 6), (1, 256, 4), (2, 128, 8), (1, 128, 6), (1, 64, 8)):
+        for form in ((0, 0, 0), (1, 0, 0), (0, 1, 0), (1, 1, 0), (1, 0, 1)):
+            assert (atom, tile_n, d) + form in have, (atom, tile_n, d, form)
 
 
 # ------------------------------------------------------------- plans -----
@@ -125,12 +137,20 @@ def test_auto_variant_choice():
     # Large square: the 2-SM atom at MMA N = 256 (fewest waves x widest tile).
     st, p = plan(8192, 8192, 8192)
     assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (2, 256, 6)
-    # Few output tiles: N = 128 tiles spread the work over more SMs, and a
-    # single wave of 1-SM tiles avoids the cluster's fixed cost.
+    # Few output tiles: 128 x 64 tiles spread the operand streams over twice
+    # as many SMs (1000^3: 128 CTAs instead of 64), and a single wave of 1-SM
+    # tiles avoids the cluster's fixed cost.
     st, p = plan(1000, 1000, 1000, lda=1008, ldb=1008, ldc=1000, out_f32=True)
-    assert (p["atom"], p["tile_n"]) == (1, 128) and p["grid"] == 64
+    assert (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 64, 8) and p["grid"] == 128
     st, p = plan(128, 128, 64)
-    assert (p["atom"], p["tile_n"], p["grid"]) == (1, 128, 1)
+    assert (p["atom"], p["tile_n"], p["grid"]) == (1, 64, 2)
+    # One row of tiles over a long K: 128 x 64 tiles give 128 CTAs (the
+    # 2-SM atom would leave half of each pair's rows empty at M = 128).
+    st, p = plan(128, 8192, 16384)
+    assert (p["atom"], p["tile_n"], p["grid"]) == (1, 64, 128)
+    # Mid-size: 1-SM, N = 256 tiles fill one wave.
+    st, p = plan(2048, 2048, 2048)
+    assert (p["atom"], p["tile_n"]) == (1, 256)
     # Several waves: the 2-SM atom's deeper ring wins.
     st, p = plan(2560, 2560, 2560)
     assert (p["atom"], p["tile_n"]) == (2, 256)
@@ -182,7 +202,10 @@ def test_plan_tma_suitability():
 
 def test_plan_budget_errors():
     assert plan(256, 256, 256, atom=2, pipe_depth=9)[0] == tp.TP_ERR_SMEM_BUDGET
-    assert plan(256, 256, 256, atom=1, pipe_depth=7)[0] == tp.TP_ERR_SMEM_BUDGET
+    assert plan(256, 256, 256, atom=1, tile_n=128, pipe_depth=7)[0] == tp.TP_ERR_SMEM_BUDGET
+    assert plan(256, 256, 256, atom=1, tile_n=64, pipe_depth=9)[0] == tp.TP_ERR_SMEM_BUDGET
+    st, p = plan(256, 256, 256, atom=1, tile_n=64, pipe_depth=8)
+    assert st == tp.TP_OK and p["pipe_depth"] == 8
     assert plan(256, 256, 256, atom=1, tile_n=256, pipe_depth=5)[0] == tp.TP_ERR_SMEM_BUDGET
     assert plan(256, 256, 256, atom=3)[0] == tp.TP_ERR_INVALID_ARG
     st, p = plan(256, 256, 256, atom=2, pipe_depth=8)
@@ -195,7 +218,7 @@ def test_splitk_workspace_arithmetic():
     with pytest.raises(tp.TPError):
         tp.tp_gemm_splitk_workspace_bytes(10, 10, 0)
     ks = [k for k in tp.tp_list_kernels() if k["splitk"]]
-    assert {(k["atom"], k["tile_n"]) for k in ks} == {(1, 128), (1, 256), (2, 128), (2, 256)}
+    assert {(k["atom"], k["tile_n"]) for k in ks} == {(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)}
     assert all(k["out_f32"] == 1 and k["conv"] == 0 for k in ks)
 
 
