@@ -44,7 +44,7 @@ def _gemm_case(i, depths):
     opts = {}
     if rng.random() < 0.5:
         opts["atom"] = rng.choice([1, 2])
-        opts["tile_n"] = rng.choice([128, 256])
+        opts["tile_n"] = rng.choice([64, 128, 256] if opts["atom"] == 1 else [128, 256])
         ds = depths.get((opts["atom"], opts["tile_n"], int(out_f32)), [])
         if ds and rng.random() < 0.5 and aligned:
             opts["pipe_depth"] = rng.choice(ds)
@@ -96,6 +96,8 @@ def _conv_case(i):
     opts = {}
     if rng.random() < 0.4:
         opts["atom"] = rng.choice([1, 2])
+        if opts["atom"] == 1 and rng.random() < 0.4:
+            opts["tile_n"] = 64
     return Nb, H, W, C, K, R, S, st, pad, out_f32, opts
 
 
