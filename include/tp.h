@@ -99,9 +99,12 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               (0 = 2048 rows of A per group: 16 tiles of the 1-SM atom,
  *               8 pair tiles of the 2-SM atom).
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM). A cap at
- *               or above the tile count (CTAs = tiles x atom) launches one
+ *               or above the work-unit count (CTAs = units x atom; units =
+ *               tiles, plus the narrow tail's extra halves) launches one
  *               work unit per cluster, i.e. a non-persistent grid that the
- *               hardware schedules in waves.
+ *               hardware schedules in waves. The narrow tail is sized by the
+ *               clusters that run at once: the cap or SMs / atom, whichever
+ *               is smaller.
  *   l2_hint:    L2 eviction priorities of the operand loads: 0 choose,
  *               1 none (no cache-hint policy), 2 A evict-last / B
  *               evict-first, 3 A evict-last, 4 B evict-first, 5 A

@@ -300,23 +300,31 @@ void normalize_splits(int64_t k_blocks, int* splits, int* kb_per_split)
 
 
 
+int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom);
+
 // Narrow tail for the 2-SM atom at N = 256: when the tiles left for the last,
-// partial wave (r = tiles mod clusters) fit twice into one wave, they run as
-// 2r half-width units, so that wave takes about half as long. A problem with
-// fewer tiles than clusters is all tail: its tiles run as half-width units on
-// twice as many clusters.
-void set_narrow_tail(tp_plan& pl, GemmParams& p, int64_t max_clusters)
+// partial wave (r = tiles mod W) fit twice into one wave, they run as 2r
+// half-width units, so that wave takes about half as long. W is the number
+// of clusters that run at once: the grid cap (max_ctas) or the GPU's SMs /
+// 2, whichever is smaller. A problem with fewer tiles than W is all tail:
+// its tiles run as half-width units on twice as many clusters. The grid is
+// W clusters (persistent), or one per unit when the cap allows as many
+// (non-persistent).
+void set_narrow_tail(tp_plan& pl, GemmParams& p, const tp_gemm_opts* o, int sm_count)
 {
     p.n_full = 0;
     p.tail_units = 0;
-    if (pl.atom != 2 || pl.tile_n != 256 || max_clusters < 2) return;
+    if (pl.atom != 2 || pl.tile_n != 256) return;
+    const int64_t cap = max_clusters_for(o, sm_count, pl.atom);
+    const int64_t wave = std::min<int64_t>(cap, std::max<int64_t>(1, sm_count / pl.atom));
+    if (wave < 2) return;
     const int64_t tiles = pl.m_tiles * pl.n_tiles;
-    const int64_t r = tiles % max_clusters;
-    if (r == 0 || 2 * r > max_clusters) return;
+    const int64_t r = tiles % wave;
+    if (r == 0 || 2 * r > wave) return;
     p.n_full = static_cast<int>(tiles - r);
     p.tail_units = static_cast<int>(2 * r);
-    const int64_t clusters = tiles >= max_clusters ? max_clusters : 2 * r;
-    pl.grid = static_cast<int>(clusters * pl.atom);
+    const int64_t units = tiles - r + 2 * r;
+    pl.grid = static_cast<int>(std::min<int64_t>(cap, units) * pl.atom);
     pl.tail_units = p.tail_units;
 }
 
@@ -483,7 +491,7 @@ int tp_gemm_plan(const void* A, const void* B, const void* C, int64_t M, int64_t
     const int st = gemm_plan_impl(A, B, C, M, N, K, lda, ldb, ldc, out_f32 ? 1 : 0, opts, sm_count, plan);
     if (st == TP_OK && plan->path == TP_PATH_MAINLOOP && !(opts && opts->no_tail)) {
         GemmParams unused{};
-        set_narrow_tail(*plan, unused, max_clusters_for(opts, sm_count, plan->atom));
+        set_narrow_tail(*plan, unused, opts, sm_count);
     }
     return st;
 }
@@ -600,7 +608,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.splits = use_splitk ? pl.splits : 1;
     p.kb_per_split = use_splitk ? kps : p.k_blocks;
     if (!use_splitk && !(opts && opts->no_tail))
-        set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
+        set_narrow_tail(pl, p, opts, dev->sm_count);
     p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
@@ -765,7 +773,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.k_blocks = static_cast<int>(pl.k_blocks);
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
-    if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, max_clusters_for(opts, dev->sm_count, pl.atom));
+    if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, opts, dev->sm_count);
     p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     pl.l2_hint = l2_mode_for(opts, pl.m_tiles, pl.n_tiles, 0.0, 0.0, false);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);

@@ -79,6 +79,7 @@ def test_atom2_conv(tile_n, out_f32):
 
 @pytest.mark.parametrize("M,N,K,max_ctas", [(1280, 512, 640, 8),     # 10 tiles on 4 clusters: 8 whole + 4 halves
                                              (2560, 2048, 384, 0),    # 80 tiles on 76 clusters: 76 + 8 halves
+                                             (2560, 2048, 384, 100000),  # the same, one cluster per unit (84)
                                              (600, 100, 448, 0),      # 3 tiles, all halves; upper halves out of N
                                              (320, 200, 448, 0)])
 @pytest.mark.parametrize("out_f32", [True, False])
@@ -100,7 +101,7 @@ def test_narrow_tail_units(M, N, K, max_ctas, out_f32):
 def test_narrow_tail_conv():
     N, H, W, C, K, R, S = 4, 20, 18, 64, 256, 3, 3   # 1440 pixels: 6 pair tiles, all halves
     x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=23)
-    y = new_out(N * H * W, K, False)   # the 2-SM / N 256 conv is compiled with a bf16 output
+    y = new_out(N * H * W, K, False)
     tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, 1, 1, atom=2, tile_n=256)
     expect_ok()
     assert tp.tp_last_plan()["tail_units"] == 12

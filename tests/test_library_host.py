@@ -229,6 +229,15 @@ def test_narrow_tail_plan():
     assert (p["atom"], p["tile_n"], p["tail_units"], p["grid"]) == (2, 256, 72, 152)
     st, p = plan(8192, 8192, 8192, no_tail=1)
     assert p["tail_units"] == 0
+    # A grid cap above the machine (non-persistent launch): the wave is still
+    # the 76 clusters that run at once, so only the 36 leftover tiles split,
+    # and each of the 988 + 72 units gets a cluster of its own.
+    st, p = plan(8192, 8192, 8192, atom=2, tile_n=256, max_ctas=100000)
+    assert (p["tail_units"], p["grid"]) == (72, 2 * 1060)
+    st, p = plan(100352, 256, 2304, atom=2, tile_n=256, max_ctas=100000)   # 392 tiles: 5 waves + 12
+    assert (p["tail_units"], p["grid"]) == (24, 2 * 404)
+    st, p = plan(100352, 256, 2304, atom=2, tile_n=256)
+    assert (p["tail_units"], p["grid"]) == (24, 152)
     # 10 tiles on 4 clusters: 8 whole, 2 left -> 4 halves.
     st, p = plan(1280, 512, 640, atom=2, tile_n=256, max_ctas=8)
     assert (p["tail_units"], p["grid"]) == (4, 8)
