@@ -49,7 +49,7 @@ def _gemm_case(i, depths):
         if ds and rng.random() < 0.5 and aligned:
             opts["pipe_depth"] = rng.choice(ds)
     if rng.random() < 0.3:
-        opts["max_ctas"] = rng.choice([2, 4, 6, 16])
+        opts["max_ctas"] = rng.choice([2, 4, 6, 16, 100000])
     if rng.random() < 0.3:
         opts["group_m"] = rng.choice([1, 2, 3])
     if rng.random() < 0.2:
