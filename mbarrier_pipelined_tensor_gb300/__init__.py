@@ -321,21 +321,49 @@ def tp_selftest_wait_timeout(limit_us: int, stream=None):
 # Tensor conveniences (still marshalling only: shapes -> sizes and pitches).
 # --------------------------------------------------------------------------
 
+def _require(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _rows_packed(t, name):
+    """A 2-D view whose rows are packed (unit stride along the last axis)."""
+    _require(t.dim() == 2, f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    _require(t.shape[1] <= 1 or t.stride(1) == 1, f"{name} must have unit stride along its last axis")
+
+
 def gemm(A, B_nk, C, stream=None, **opts):
     """C (M x N, bf16 or fp32) = A (M x K) . B, B given as an N x K tensor
-    (i.e. K x N column-major). Row pitches come from the tensors' strides."""
+    (i.e. K x N column-major). Row pitches come from the tensors' strides;
+    each row must be packed (a transposed view is rejected, not copied)."""
+    for t, name in ((A, "A"), (B_nk, "B_nk"), (C, "C")):
+        _rows_packed(t, name)
     M, K = A.shape
     N = B_nk.shape[0]
+    _require(B_nk.shape[1] == K, f"B_nk is {tuple(B_nk.shape)}, expected ({N}, {K})")
+    _require(tuple(C.shape) == (M, N), f"C is {tuple(C.shape)}, expected ({M}, {N})")
+    _require(str(A.dtype).endswith("bfloat16") and str(B_nk.dtype).endswith("bfloat16"), "A and B_nk must be bf16")
+    _require(str(C.dtype).endswith("bfloat16") or str(C.dtype).endswith("float32"), "C must be bf16 or fp32")
     out_f32 = str(C.dtype).endswith("float32")
-    tp_gemm_bf16_ex(A, B_nk, C, M, N, K, A.stride(0), B_nk.stride(0), C.stride(0), out_f32=out_f32,
-                    stream=stream, **opts)
+    tp_gemm_bf16_ex(A, B_nk, C, M, N, K, max(A.stride(0), K), max(B_nk.stride(0), K), max(C.stride(0), N),
+                    out_f32=out_f32, stream=stream, **opts)
     return C
 
 
 def conv2d_fprop(x, w, y, stride=1, pad=0, stream=None, **opts):
-    """y (N x P x Q x K) = conv(x (N x H x W x C), w (K x R x S x C))."""
+    """y (N x P x Q x K) = conv(x (N x H x W x C), w (K x R x S x C)), all
+    three contiguous (NHWC / KRSC / NPQK); y may also be (N*P*Q) x K."""
+    _require(x.dim() == 4 and w.dim() == 4, "x and w must be 4-D (NHWC, KRSC)")
     N, H, W, C = x.shape
-    K, R, S, _ = w.shape
+    K, R, S, Cw = w.shape
+    _require(Cw == C, f"w has {Cw} input channels, x has {C}")
+    P = (H + 2 * pad - R) // stride + 1
+    Q = (W + 2 * pad - S) // stride + 1
+    _require(y.numel() == N * P * Q * K and y.shape[-1] == K, f"y must hold {N}x{P}x{Q}x{K} outputs")
+    for t, name in ((x, "x"), (w, "w"), (y, "y")):
+        _require(t.is_contiguous(), f"{name} must be contiguous")
+    _require(str(x.dtype).endswith("bfloat16") and str(w.dtype).endswith("bfloat16"), "x and w must be bf16")
+    _require(str(y.dtype).endswith("bfloat16") or str(y.dtype).endswith("float32"), "y must be bf16 or fp32")
     out_f32 = str(y.dtype).endswith("float32")
     tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, out_f32=out_f32, stream=stream, **opts)
     return y

@@ -451,3 +451,27 @@ def test_gemm_host_buffers_pageable():
     expect_ok()
     ref, ab = oracle.gemm(A, B, M, N, K, K, K)
     check_against_oracle(c_h.astype(np.float64), ref, ab, True, "pageable host buffers")
+
+
+# ------------------------------------------------ torch-facing wrappers ---
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_convenience_wrappers(out_f32):
+    # tp.gemm / tp.conv2d_fprop take shapes and pitches from the tensors:
+    # a padded-pitch A (a column slice of a wider buffer) and a flat y.
+    M, N, K = 300, 200, 448
+    A, B = datagen.gemm_operands(M, N, K, seed=91, lda=456)
+    a_full = dev_bf16(A)                     # M x 456, the first K columns used
+    b = dev_bf16(B)
+    c = new_out(M, N, out_f32)
+    tp.gemm(a_full[:, :K], b, c)
+    expect_ok()
+    ref, ab = oracle.gemm(A, B, M, N, K, 456, K)
+    check_against_oracle(host_f64(c), ref, ab, out_f32, "tp.gemm")
+    Nb, H, W, C, Kc, R, S = 2, 9, 7, 64, 72, 3, 3
+    x, w = datagen.conv_operands(Nb, H, W, C, Kc, R, S, seed=92)
+    y = new_out(Nb * H * W, Kc, out_f32)
+    tp.conv2d_fprop(dev_bf16(x).view(Nb, H, W, C), dev_bf16(w).view(Kc, R, S, C), y, stride=1, pad=1)
+    expect_ok()
+    ref, ab = oracle.conv(x, w, Nb, H, W, C, Kc, R, S, 1, 1)
+    check_against_oracle(host_f64(y), ref, ab, out_f32, "tp.conv2d_fprop")

@@ -287,3 +287,29 @@ def test_l2_priority_choice():
     assert mode(8192, 8192, 8192, l2_hint=4) == 4
     assert mode(8192, 8192, 8192, l2_hint=7) == 7   # explicit evict_normal policy
     assert plan(128, 128, 128, l2_hint=8)[0] == tp.TP_ERR_INVALID_ARG
+
+
+def test_convenience_wrappers_reject_bad_views():
+    # The torch-facing wrappers take pitches from strides; views they cannot
+    # describe are refused before anything reaches the library.
+    torch = pytest.importorskip("torch")
+    bf = torch.bfloat16
+    A = torch.zeros(64, 32, dtype=bf)
+    B = torch.zeros(48, 32, dtype=bf)
+    C = torch.zeros(64, 48, dtype=bf)
+    with pytest.raises(ValueError):
+        tp.gemm(torch.zeros(32, 64, dtype=bf).t(), B, C)            # transposed A
+    with pytest.raises(ValueError):
+        tp.gemm(A, torch.zeros(48, 16, dtype=bf), C)                 # B of the wrong K
+    with pytest.raises(ValueError):
+        tp.gemm(A, B, torch.zeros(64, 40, dtype=bf))                 # C of the wrong N
+    with pytest.raises(ValueError):
+        tp.gemm(A.float(), B, C)                                     # fp32 operand
+    x = torch.zeros(2, 8, 8, 16, dtype=bf)
+    w = torch.zeros(32, 3, 3, 16, dtype=bf)
+    with pytest.raises(ValueError):
+        tp.conv2d_fprop(x, torch.zeros(32, 3, 3, 8, dtype=bf), torch.zeros(2, 8, 8, 32, dtype=bf), pad=1)
+    with pytest.raises(ValueError):
+        tp.conv2d_fprop(x.permute(0, 2, 1, 3), w, torch.zeros(2, 8, 8, 32, dtype=bf), pad=1)   # not NHWC-packed
+    with pytest.raises(ValueError):
+        tp.conv2d_fprop(x, w, torch.zeros(2, 6, 6, 32, dtype=bf), pad=1)                       # wrong P, Q
