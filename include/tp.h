@@ -12,6 +12,12 @@
  *  - The return value reports what the host can see: invalid arguments, a
  *    descriptor the driver rejects, a launch error. Device-side failures (a
  *    bounded barrier wait that gave up) surface through tp_device_status.
+ *  - Entry points may be called from several host threads at once: the
+ *    per-device state is set up once under a lock, and the last-plan and
+ *    last-CUDA-error records are per thread. The device status record is
+ *    per GPU, so a tp_device_status call sees (and clears) a failure of any
+ *    thread's launch on that GPU. tp_gemm_bf16_splitk_noalloc shares one
+ *    workspace per GPU (see there).
  *  - bf16 is IEEE-style bfloat16; results are rounded to nearest even.
  *  - Empty problems (a zero M, N, rows or cols) are a no-op returning TP_OK.
  *    Negative sizes, a leading dimension below the row width, or a NULL

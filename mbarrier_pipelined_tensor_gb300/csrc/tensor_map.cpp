@@ -36,6 +36,16 @@ void resolve()
     });
 }
 
+// The encode functions are driver calls and need a current context. A host
+// thread that has not touched the CUDA runtime yet has none (reading the
+// current device does not create it), so make the device's primary context
+// current first, as every runtime call does implicitly.
+void bind_primary_context()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaSetDevice(dev);
+}
+
 uint32_t elem_bytes(CUtensorMapDataType t)
 {
     switch (t) {
@@ -139,6 +149,7 @@ int encode_tiled(CUtensorMap* out, const TiledDesc& d)
     resolve();
     if (!g_found) return ST_CUDA;
     if (!tiled_ok(d)) return ST_INVALID_ARG;
+    bind_primary_context();
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = g_tiled(out, d.dtype, d.rank, d.base, reinterpret_cast<const cuuint64_t*>(d.dims),
                          reinterpret_cast<const cuuint64_t*>(d.strides_bytes),
@@ -157,6 +168,7 @@ int encode_im2col(CUtensorMap* out, const Im2colDesc& d)
     if ((reinterpret_cast<uintptr_t>(d.base) & 15u) != 0) return ST_INVALID_ARG;
     for (int i = 0; i < 3; ++i)
         if (d.strides_bytes[i] % 16 != 0) return ST_INVALID_ARG;
+    bind_primary_context();
     CUresult r = g_im2col(out, d.dtype, 4, d.base, reinterpret_cast<const cuuint64_t*>(d.dims),
                           reinterpret_cast<const cuuint64_t*>(d.strides_bytes), d.lower, d.upper, d.channels,
                           d.pixels, reinterpret_cast<const cuuint32_t*>(d.elem_strides),

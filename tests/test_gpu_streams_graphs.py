@@ -84,3 +84,51 @@ def test_concurrent_streams_match_serial():
     expect_ok()
     for o1, o2 in zip(serial, conc):
         _same(o1, o2)
+
+
+def test_concurrent_host_threads():
+    # Four host threads call the library at once, each on its own stream
+    # (ctypes releases the GIL, so planning, descriptor encoding and launches
+    # really overlap). Every result equals the single-threaded one bit for bit.
+    import threading
+    cases = [(320, 200, 448, {}), (1000, 1000, 1000, {}), (512, 768, 640, dict(atom=2, tile_n=256)),
+             (256, 512, 1024, dict(atom=1, tile_n=64))]
+    data = []
+    for i, (M, N, K, o) in enumerate(cases):
+        A, B = datagen.gemm_operands(M, N, K, seed=300 + i)
+        a, b = dev_bf16(A), dev_bf16(B)
+        ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        tp.tp_gemm_bf16_ex(a, b, ref, M, N, K, K, K, N, **o)
+        data.append((a, b, ref))
+    torch.cuda.synchronize()
+    expect_ok()
+    errors = []
+
+    def worker(i):
+        try:
+            M, N, K, o = cases[i]
+            a, b, ref = data[i]
+            c = torch.empty_like(ref)
+            # The first call comes from a thread that has made no CUDA call
+            # yet (no current context): encoding C's new tensor map must
+            # still work.
+            tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, **o)
+            torch.cuda.current_stream().synchronize()
+            st = torch.cuda.Stream()
+            for _ in range(25):
+                tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, stream=st, **o)
+                plan = tp.tp_last_plan()   # this thread's own call
+                assert (plan["m_tiles"], plan["k_blocks"]) == (-(-M // (128 * plan["atom"])), -(-K // 64))
+            st.synchronize()
+            if not torch.equal(c, ref):
+                errors.append(f"case {i}: result differs from the single-threaded run")
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(f"case {i}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    expect_ok()
