@@ -313,3 +313,42 @@ def test_convenience_wrappers_reject_bad_views():
         tp.conv2d_fprop(x.permute(0, 2, 1, 3), w, torch.zeros(2, 8, 8, 32, dtype=bf), pad=1)   # not NHWC-packed
     with pytest.raises(ValueError):
         tp.conv2d_fprop(x, w, torch.zeros(2, 6, 6, 32, dtype=bf), pad=1)                       # wrong P, Q
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include "tp.h"
+int main(void)
+{
+    tp_gemm_opts o = {0};
+    tp_plan pl;
+    int64_t b = 0;
+    int st = tp_query_smem_bytes(2, 6, 256, 0, &b);
+    printf("%d %lld %s\n", st, (long long)b, tp_status_string(st));
+    st = tp_gemm_plan((void*)0x100000, (void*)0x100000, (void*)0x100000, 8192, 8192, 8192, 8192, 8192, 8192, 0,
+                      &o, 152, &pl);
+    printf("%d %d %d %d %d\n", st, pl.atom, pl.tile_n, pl.pipe_depth, pl.grid);
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    # include/tp.h is a C header: a C99 program compiles against it without
+    # warnings (-pedantic -Werror), links libtp.so and plans the 8192^3 GEMM
+    # without a GPU.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(tp.LIB_PATH)
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", f"-I{ROOT}/include", str(src),
+                        f"-L{libdir}", "-ltp", f"-Wl,-rpath,{libdir}", "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split("\n")[:2] == ["0 230656 TP_OK", "0 2 256 6 152"]
