@@ -620,7 +620,8 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD.format(n=M), "sample": sample},
+            "config": {"workload": WORKLOAD.format(n=M), "M": M, "N": N, "K": K, "sample": sample,
+                       "parallelism": f"cpu oracle, {oracle.threads()} threads"},
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
