@@ -131,6 +131,9 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               nanoseconds each role spent waiting on each barrier and its
  *               active span, per CTA (the pair's leader holds the MMA
  *               issuer's counters). Tracing adds a timer read per wait.
+ *   events:     NULL, or a caller-owned, zeroed device buffer of
+ *               TP_EVENT_SLOTS x (CTAs of the launch) uint64: the per-unit
+ *               event timeline below. Both buffers may be given at once.
  * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
  * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
  * "StageCount<9> fails the capacity assert"; a combination that fits but is
@@ -145,6 +148,7 @@ typedef struct {
     int l2_hint;
     int no_tail;
     uint64_t* trace;
+    uint64_t* events;
 } tp_gemm_opts;
 
 /* Role-timeline counters per CTA (tp_gemm_opts.trace), in this order:
@@ -155,6 +159,21 @@ typedef struct {
  * small share of the MMA span ("B200 Tma Pipeline Designer", step 8: copies
  * genuinely overlapping tensor-core work). */
 #define TP_TRACE_SLOTS 8
+
+/* Per-unit event timeline per CTA (tp_gemm_opts.events): for the CTA's first
+ * TP_EVENT_UNITS work units (output tiles, split-K slices or half-width tail
+ * units, in the order it runs them), TP_EVENTS_PER_UNIT slots each, in this
+ * order: producer about to wait for the unit's first free stage, producer
+ * issued the unit's last loads, MMA issuer found the unit's accumulator free,
+ * MMA issuer issued the unit's last MMAs, epilogue (warp 2) found the
+ * accumulator complete, epilogue handed it back, epilogue issued the unit's
+ * last store; all globaltimer nanoseconds. The last slot holds the unit's
+ * index. The MMA events of a 2-SM pair are in its leader CTA's slots; the
+ * plain-load producer records no producer events. Slots of units the CTA
+ * did not run stay as the caller left them. */
+#define TP_EVENTS_PER_UNIT 8
+#define TP_EVENT_UNITS 8
+#define TP_EVENT_SLOTS (TP_EVENTS_PER_UNIT * TP_EVENT_UNITS)
 
 /* tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit choices (opts may be NULL).
  * out_f32 selects a float C (1) or a bf16 C (0). */

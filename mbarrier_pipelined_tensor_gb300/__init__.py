@@ -46,7 +46,7 @@ TP_PATH_VEC_TRANSPOSE = 7
 class tp_gemm_opts(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int), ("l2_hint", ctypes.c_int),
-                ("no_tail", ctypes.c_int), ("trace", ctypes.c_void_p)]
+                ("no_tail", ctypes.c_int), ("trace", ctypes.c_void_p), ("events", ctypes.c_void_p)]
 
 
 class tp_copy_opts(ctypes.Structure):
@@ -174,10 +174,16 @@ def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
 TRACE_SLOTS = 8
 TRACE_NAMES = ("producer_span", "producer_wait_empty", "mma_span", "mma_wait_full", "mma_wait_acc_empty",
                "epilogue_span", "epilogue_wait_acc_full", "units")
+EVENTS_PER_UNIT = 8
+EVENT_UNITS = 8
+EVENT_SLOTS = EVENTS_PER_UNIT * EVENT_UNITS
+EVENT_NAMES = ("producer_start", "producer_end", "mma_start", "mma_end", "epilogue_ready", "epilogue_released",
+               "epilogue_stored", "unit")
 
 
-def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_tail=0, trace=None):
-    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint, int(bool(no_tail)), _ptr(trace))
+def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_tail=0, trace=None, events=None):
+    return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint, int(bool(no_tail)), _ptr(trace),
+                        _ptr(events))
 
 
 def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):

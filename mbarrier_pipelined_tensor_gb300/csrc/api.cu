@@ -15,6 +15,7 @@
 #include "tp.h"
 
 static_assert(TP_TRACE_SLOTS == tp::kTraceSlots, "trace layout");
+static_assert(TP_EVENT_SLOTS == tp::kEventSlots && TP_EVENTS_PER_UNIT == tp::kEventsPerUnit, "event layout");
 
 namespace tp {
 const KernelEntry* table_mainloop_cg1(int* n);
@@ -613,6 +614,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
+    p.events = opts ? reinterpret_cast<unsigned long long*>(opts->events) : nullptr;
     p.C = use_splitk ? ws : C;
     p.ldc_bytes = use_splitk ? ldw * 4 : ldc * eb;
     p.wait = WaitCtl{dev->status, t_selftest_limit_ns ? t_selftest_limit_ns : wait_limit_ns()};
@@ -785,6 +787,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.conv_cblocks = static_cast<int>(cblocks);
     p.n_tma = (ldg || !y_tma) ? 0 : static_cast<int>(K);  // TMA stores: rows are whole 16-byte granules
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
+    p.events = opts ? reinterpret_cast<unsigned long long*>(opts->events) : nullptr;
     p.C = y;
     p.ldc_bytes = K * eb_out;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};

@@ -118,6 +118,8 @@ struct GemmParams {
     // Optional role timeline: kTraceSlots counters per CTA (nanoseconds,
     // accumulated with atomicAdd), or nullptr.
     unsigned long long* trace;
+    // Optional per-unit event timeline: kEventSlots per CTA, or nullptr.
+    unsigned long long* events;
     // Self-test only (tp_selftest_mainloop_withheld_arrival): 1 makes the
     // producer withhold the expect_tx arrival of its first stage while still
     // issuing its loads, so the consumer's bounded wait must give up.
@@ -137,6 +139,23 @@ enum : int {
     TRACE_UNITS,                  // work units this CTA's MMA issuer processed
     kTraceSlots
 };
+
+// Per-unit event timeline (GemmParams::events): for each CTA's first
+// kEventUnits work units, kEventsPerUnit slots of globaltimer nanoseconds,
+// taken at the unit boundaries of each role, plus the unit's index.
+enum : int {
+    EV_PRODUCER_START = 0,  // producer: about to wait for the unit's first free stage
+    EV_PRODUCER_END,        // producer: the unit's last loads issued
+    EV_MMA_START,           // MMA issuer: the unit's accumulator is free
+    EV_MMA_END,             // MMA issuer: the unit's last MMAs issued
+    EV_EPI_READY,           // epilogue (warp 2): the accumulator is complete
+    EV_EPI_RELEASED,        // epilogue (warp 2): accumulator read, handed back
+    EV_EPI_STORED,          // epilogue (warp 2): the unit's last store issued
+    EV_UNIT,                // the work unit's index (not a time)
+    kEventsPerUnit
+};
+constexpr int kEventUnits = 8;
+constexpr int kEventSlots = kEventsPerUnit * kEventUnits;
 
 struct CopyParams {
     int tiles_x, tiles_y;      // tiles along columns / rows

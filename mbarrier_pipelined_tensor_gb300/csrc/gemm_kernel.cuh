@@ -194,6 +194,13 @@ __device__ __forceinline__ void trace_add(const GemmParams& p, int slot, unsigne
     if (p.trace) atomicAdd(p.trace + static_cast<size_t>(blockIdx.x) * kTraceSlots + slot, v);
 }
 
+// Per-unit event timeline: this CTA's slot for event `ev` of its lt-th unit.
+__device__ __forceinline__ void event_at(const GemmParams& p, int lt, int ev, unsigned long long v)
+{
+    if (p.events && lt < kEventUnits)
+        p.events[static_cast<size_t>(blockIdx.x) * kEventSlots + lt * kEventsPerUnit + ev] = v;
+}
+
 // Bounded wait that charges its duration to a timeline slot.
 template <bool CL>
 __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -328,8 +335,9 @@ __global__ void __launch_bounds__(192, 1)
                 const uint64_t pol_b = HB ? make_l2_policy(p.l2_b) : 0;
                 const uint32_t fb0 = CL ? mapa_shared(full_bar(0), 0) : full_bar(0);
                 bool arrive = !p.withhold_first_arrival;  // the self test withholds the very first arrival
-                for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                for (int u = cluster_id, plt = 0; ok && u < num_units; u += num_clusters, ++plt) {
                     const Unit w = unit_of(u, num_tiles, p);
+                    if (p.events) event_at(p, plt, EV_PRODUCER_START, globaltimer_ns());
                     int mt, nt;
                     tile_coords(w.tile, p, mt, nt);
                     const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
@@ -403,6 +411,10 @@ __global__ void __launch_bounds__(192, 1)
                             ph ^= 1u;
                         }
                     }
+                    if (p.events) {
+                        event_at(p, plt, EV_PRODUCER_END, globaltimer_ns());
+                        event_at(p, plt, EV_UNIT, static_cast<unsigned long long>(u));
+                    }
                 }
             };
             // A load carries a cache-hint policy only when its operand's
@@ -462,6 +474,7 @@ __global__ void __launch_bounds__(192, 1)
                     const int b = lt & 1;
                     const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
                     if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
+                    if (p.events) event_at(p, lt, EV_MMA_START, globaltimer_ns());
                     tcgen05_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                     const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
@@ -488,6 +501,7 @@ __global__ void __launch_bounds__(192, 1)
                         }
                     }
                     if (!ok) break;
+                    if (p.events) event_at(p, lt, EV_MMA_END, globaltimer_ns());
                     if constexpr (CL) umma_commit_pair(accf_bar(b), 0x3);
                     else umma_commit(accf_bar(b));
                 }
@@ -520,6 +534,7 @@ __global__ void __launch_bounds__(192, 1)
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
             if (!timed_wait<CL>(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
+            if (p.events && warp == 2 && lane == 0) event_at(p, lt, EV_EPI_READY, globaltimer_ns());
             tcgen05_fence_after();
             int mt, nt;
             tile_coords(w.tile, p, mt, nt);
@@ -567,6 +582,9 @@ __global__ void __launch_bounds__(192, 1)
                     tcgen05_fence_before();
                     __syncwarp();
                     if (lane == 0) {
+                        // stamped before the arrival, so the MMA issuer cannot
+                        // see the accumulator free before this time
+                        if (p.events && warp == 2) event_at(p, lt, EV_EPI_RELEASED, globaltimer_ns());
                         if constexpr (CL) mbar_arrive_cluster(acce_target);
                         else mbar_arrive(acce_target);
                     }
@@ -614,6 +632,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            if (p.events && warp == 2 && lane == 0) event_at(p, lt, EV_EPI_STORED, globaltimer_ns());
         }
         if (p.trace && warp == 2 && lane == 0) {
             trace_add(p, TRACE_EPI_SPAN, globaltimer_ns() - t_start);

@@ -129,3 +129,46 @@ def test_role_timeline(atom, tile_n):
     assert issuers[:, 7].sum() == tiles + plan["tail_units"] // 2  # whole tiles, plus 2 units per tail tile
     for rows, span, wait in ((t, 0, 1), (issuers, 2, 3), (issuers, 2, 4), (t, 5, 6)):
         assert np.all(rows[:, span] > 0) and np.all(rows[:, wait] <= rows[:, span])
+
+
+@pytest.mark.parametrize("atom,tile_n", [(2, 256), (2, 128), (1, 128), (1, 64)])
+def test_event_timeline(atom, tile_n):
+    # The per-unit event timeline on a small grid (many units per CTA): every
+    # CTA runs units cluster_id, cluster_id + clusters, ... in that order,
+    # each role's events are in order, and the two TMEM accumulators
+    # alternate: a unit's MMAs start only after the epilogue warps of its
+    # CTA (both CTAs of a pair) handed back the accumulator of the unit two
+    # before it.
+    M, N, K = 2560, 2048, 1024
+    A, B = datagen.gemm_operands(M, N, K, seed=84)
+    a, b = dev_bf16(A), dev_bf16(B)
+    c = new_out(M, N, False)
+    opts = dict(atom=atom, tile_n=tile_n, max_ctas=16)
+    tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, **opts)
+    plan = tp.tp_last_plan()
+    grid = plan["grid"]
+    ev = torch.zeros(grid * tp.EVENT_SLOTS, dtype=torch.int64, device="cuda")
+    tp.tp_gemm_bf16_ex(a, b, c, M, N, K, K, K, N, events=ev, **opts)
+    expect_ok()
+    e = ev.view(grid, tp.EVENT_UNITS, tp.EVENTS_PER_UNIT).cpu().numpy().astype(np.int64)
+    P0, P1, M0, M1, E0, E1, E2, U = range(8)
+    clusters = grid // atom
+    units = plan["m_tiles"] * plan["n_tiles"] + plan["tail_units"] // 2
+    assert units >= clusters * tp.EVENT_UNITS   # every CTA fills all its event slots
+    for cta in range(grid):
+        cid, leader = cta // atom, cta - (cta // atom) * atom == 0
+        lead = cid * atom
+        for k in range(tp.EVENT_UNITS):
+            r = e[cta, k]
+            assert r[U] == cid + k * clusters
+            assert 0 < r[P0] <= r[P1]
+            assert 0 < r[E0] <= r[E1] <= r[E2]
+            m = e[lead, k]
+            assert 0 < m[M0] <= m[M1] <= r[E0]      # accumulator complete only after its last MMAs
+            if k >= 2:
+                for peer in range(lead, lead + atom):
+                    assert e[peer, k - 2, E1] <= m[M0], (cta, k)
+        if not leader:
+            assert np.all(e[cta, :, [M0, M1]] == 0)   # the MMA issuer runs on the pair's leader
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K, rows=np.arange(0, M, 97))
+    check_against_oracle(host_f64(c)[::97], ref, ab, False, "events run")
