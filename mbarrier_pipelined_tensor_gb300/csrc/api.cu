@@ -578,6 +578,13 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
                      {static_cast<uint64_t>(K), static_cast<uint64_t>(N)}, {static_cast<uint64_t>(ldb) * 2},
                      {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
         if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db))) return st;
+        L.mapBh = L.mapB;
+        if (pl.atom == 2 && pl.tile_n == 256 && !use_splitk) {
+            // the narrow tail's half-width units: half of each CTA's B rows
+            TiledDesc dbh = db;
+            dbh.box[1] = static_cast<uint32_t>(b_rows / 2);
+            if ((st = encode_tiled(&L.mapBh, dbh))) return st;
+        }
         if (use_splitk) {
             TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws,
                          {static_cast<uint64_t>(ldw), static_cast<uint64_t>(M), static_cast<uint64_t>(pl.splits)},
@@ -754,6 +761,12 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
                  {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
                  {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
     if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw))) return st;
+    L.mapBh = L.mapB;
+    if (pl.atom == 2 && pl.tile_n == 256) {
+        TiledDesc dwh = dw;
+        dwh.box[2] = static_cast<uint32_t>(b_rows / 2);
+        if ((st = encode_tiled(&L.mapBh, dwh))) return st;
+    }
     if (y_tma) {
         if ((st = encode_tiled(&L.mapC, dy))) return st;
     } else {

@@ -194,6 +194,7 @@ struct KernelKey {
 
 struct GemmLaunch {
     CUtensorMap mapA, mapB, mapC;
+    CUtensorMap mapBh;  // B with half-height boxes: the 2-SM, N = 256 narrow tail
     GemmParams params;
     int grid;
     cudaStream_t stream;

@@ -54,6 +54,9 @@ struct MainloopCfg {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // the leader's expect_tx covers the pair
+    // A half-width unit (the 2-SM, N = 256 narrow tail) loads half of each
+    // CTA's B rows through a half-height box.
+    static constexpr int TX_HALF_BYTES = (A_BYTES + B_BYTES / 2) * CG;
     static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
     static constexpr int EPI_COLS = 128 / OUT_BYTES;  // columns per 128-byte staging row
     static constexpr int EPI_WARPS = 4;
@@ -216,7 +219,8 @@ __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, ui
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
 __global__ void __launch_bounds__(192, 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                    const __grid_constant__ CUtensorMap mapC, const GemmParams p)
+                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapBh,
+                    const GemmParams p)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
     constexpr bool CL = (CG == 2);
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(192, 1)
             prefetch_tensormap(&mapA);
             prefetch_tensormap(&mapB);
             prefetch_tensormap(&mapC);
+            if (CG == 2 && BN == 256 && p.tail_units > 0) prefetch_tensormap(&mapBh);
         }
     }
     if (warp == 1) {
@@ -345,6 +350,9 @@ __global__ void __launch_bounds__(192, 1)
                     // starting at its half; the B box (BN/2 rows) loads them first.
                     const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
                                                  : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
+                    // half-width units (2-SM, N = 256 only) load B through the half-height box
+                    const bool hu = CG == 2 && BN == 256 && w.half >= 0;
+                    const CUtensorMap* const mB = hu ? &mapBh : &mapB;
                     [[maybe_unused]] int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
                     if constexpr (CONV) {
                         const int pq = p.conv_P * p.conv_Q;
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(192, 1)
                             break;
                         }
                         const uint32_t fb = fb0 + 8u * static_cast<uint32_t>(s);
-                        if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), Cfg::TX_BYTES);
+                        if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), hu ? Cfg::TX_HALF_BYTES : Cfg::TX_BYTES);
                         arrive = true;
                         const uint32_t dA = sA + s * Cfg::A_BYTES;
                         const uint32_t dB = sB + s * Cfg::B_BYTES;
@@ -375,13 +383,13 @@ __global__ void __launch_bounds__(192, 1)
                             if constexpr (CL) {
                                 if constexpr (HA) tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh, pol_a);
                                 else tma_load_im2col_4d_pair(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh);
-                                if constexpr (HB) tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row, pol_b);
-                                else tma_load_3d_pair(dB, &mapB, fb, c0, rs, n_row);
+                                if constexpr (HB) tma_load_3d_pair(dB, mB, fb, c0, rs, n_row, pol_b);
+                                else tma_load_3d_pair(dB, mB, fb, c0, rs, n_row);
                             } else {
                                 if constexpr (HA) tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh, pol_a);
                                 else tma_load_im2col_4d(dA, &mapA, fb, c0, base_w, base_h, img, ow, oh);
-                                if constexpr (HB) tma_load_3d(dB, &mapB, fb, c0, rs, n_row, pol_b);
-                                else tma_load_3d(dB, &mapB, fb, c0, rs, n_row);
+                                if constexpr (HB) tma_load_3d(dB, mB, fb, c0, rs, n_row, pol_b);
+                                else tma_load_3d(dB, mB, fb, c0, rs, n_row);
                             }
                             if (++cb == p.conv_cblocks) {
                                 cb = 0;
@@ -396,13 +404,13 @@ __global__ void __launch_bounds__(192, 1)
                             if constexpr (CL) {
                                 if constexpr (HA) tma_load_2d_pair(dA, &mapA, fb, kx, m_row, pol_a);
                                 else tma_load_2d_pair(dA, &mapA, fb, kx, m_row);
-                                if constexpr (HB) tma_load_2d_pair(dB, &mapB, fb, kx, n_row, pol_b);
-                                else tma_load_2d_pair(dB, &mapB, fb, kx, n_row);
+                                if constexpr (HB) tma_load_2d_pair(dB, mB, fb, kx, n_row, pol_b);
+                                else tma_load_2d_pair(dB, mB, fb, kx, n_row);
                             } else {
                                 if constexpr (HA) tma_load_2d(dA, &mapA, fb, kx, m_row, pol_a);
                                 else tma_load_2d(dA, &mapA, fb, kx, m_row);
-                                if constexpr (HB) tma_load_2d(dB, &mapB, fb, kx, n_row, pol_b);
-                                else tma_load_2d(dB, &mapB, fb, kx, n_row);
+                                if constexpr (HB) tma_load_2d(dB, mB, fb, kx, n_row, pol_b);
+                                else tma_load_2d(dB, mB, fb, kx, n_row);
                             }
                         }
                         ++issued;
@@ -673,7 +681,7 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.params);
+    return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params);
 }
 
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
