@@ -158,15 +158,19 @@ def _check(st: int, where: str) -> None:
 
 
 def tp_status_string(status: int) -> str:
+    """Name of a TP_* status code."""
     return _lib.tp_status_string(status).decode()
 
 
 def tp_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
+    """C (bf16, M x N, pitch ldc) = A (M x K, pitch lda) . B (stored N x K, pitch ldb); pitches in
+    elements. Asynchronous on `stream`; raises TPError on a host-visible error."""
     _check(_lib.tp_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, _stream(stream)),
            "tp_gemm_bf16")
 
 
 def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
+    """tp_gemm_bf16 with the fp32 accumulator written to a float C."""
     _check(_lib.tp_gemm_bf16_f32(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, _stream(stream)),
            "tp_gemm_bf16_f32")
 
@@ -187,6 +191,8 @@ def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_t
 
 
 def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):
+    """tp_gemm_bf16 / tp_gemm_bf16_f32 with explicit mainloop choices (atom, pipe_depth, tile_n,
+    group_m, max_ctas, l2_hint, no_tail, trace, events; all optional, 0 = choose)."""
     o = _opts(**opts)
     _check(_lib.tp_gemm_bf16_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, lda, ldb, ldc, int(bool(out_f32)),
                                 ctypes.byref(o), _stream(stream)), "tp_gemm_bf16_ex")
@@ -194,6 +200,8 @@ def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None,
 
 def tp_gemm_bf16_splitk(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, splits=0, workspace=None,
                         workspace_bytes=0, stream=None, **opts):
+    """The GEMM with K split into `splits` slices (0 = choose) whose fp32 partials go to the
+    caller's `workspace` (tp_gemm_splitk_workspace_bytes) and are summed into C by a second kernel."""
     o = _opts(**opts)
     if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
         workspace_bytes = workspace.numel() * workspace.element_size()
@@ -203,6 +211,7 @@ def tp_gemm_bf16_splitk(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, splits=0
 
 
 def tp_gemm_splitk_workspace_bytes(M, N, splits) -> int:
+    """Workspace bytes tp_gemm_bf16_splitk needs for M x N with `splits` slices."""
     b = _I64()
     _check(_lib.tp_gemm_splitk_workspace_bytes(M, N, splits, ctypes.byref(b)), "tp_gemm_splitk_workspace_bytes")
     return int(b.value)
@@ -227,15 +236,20 @@ def tp_gemm_bf16_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, 
 
 
 def tp_gemm_splitk_noalloc_capacity() -> int:
+    """Bytes of the in-library split-K workspace of each GPU."""
     return int(_lib.tp_gemm_splitk_noalloc_capacity())
 
 
 def tp_conv2d_fprop_bf16(x, w, y, N, H, W, C, K, R, S, stride, pad, stream=None):
+    """y (N x P x Q x K, bf16) = conv(x (N x H x W x C), w (K x R x S x C)): cross-correlation,
+    zero padding `pad`, `stride`; all three tensors packed NHWC / KRSC / NPQK."""
     _check(_lib.tp_conv2d_fprop_bf16(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad,
                                      _stream(stream)), "tp_conv2d_fprop_bf16")
 
 
 def tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, out_f32=False, stream=None, **opts):
+    """tp_conv2d_fprop_bf16 with an fp32 output option and the same mainloop choices as
+    tp_gemm_bf16_ex."""
     o = _opts(**opts)
     _check(_lib.tp_conv2d_fprop_bf16_ex(_ptr(x), _ptr(w), _ptr(y), N, H, W, C, K, R, S, stride, pad,
                                         int(bool(out_f32)), ctypes.byref(o), _stream(stream)),
@@ -243,23 +257,30 @@ def tp_conv2d_fprop_bf16_ex(x, w, y, N, H, W, C, K, R, S, stride, pad, out_f32=F
 
 
 def tp_tma_copy_2d(src, dst, rows, cols, ld, stream=None):
+    """dst = src, bit for bit: rows x cols 2-byte elements, both with row pitch `ld` elements."""
     _check(_lib.tp_tma_copy_2d(_ptr(src), _ptr(dst), rows, cols, ld, _stream(stream)), "tp_tma_copy_2d")
 
 
 def tp_tma_copy_2d_ex(src, dst, rows, cols, ld, stream=None, box_cols=0, box_rows=0, stages=0,
                       ctas_per_sm=0, force_vec=False):
+    """tp_tma_copy_2d with explicit ring choices (TMA box, stages, CTAs per SM, or the
+    vectorized copy)."""
     o = tp_copy_opts(box_cols, box_rows, stages, ctas_per_sm, int(bool(force_vec)))
     _check(_lib.tp_tma_copy_2d_ex(_ptr(src), _ptr(dst), rows, cols, ld, ctypes.byref(o), _stream(stream)),
            "tp_tma_copy_2d_ex")
 
 
 def tp_tma_transpose_2d(src, dst, rows, cols, ld_src, ld_dst, stream=None):
+    """dst[c][r] = src[r][c], bit for bit: src rows x cols (pitch ld_src), dst cols x rows
+    (pitch ld_dst), 2-byte elements."""
     _check(_lib.tp_tma_transpose_2d(_ptr(src), _ptr(dst), rows, cols, ld_src, ld_dst, _stream(stream)),
            "tp_tma_transpose_2d")
 
 
 def tp_tma_transpose_2d_ex(src, dst, rows, cols, ld_src, ld_dst, stream=None, stages=0, ctas_per_sm=0,
                            force_vec=False):
+    """tp_tma_transpose_2d with explicit ring choices (stages, CTAs per SM, or the
+    shared-memory tile fallback)."""
     o = tp_copy_opts(0, 0, stages, ctas_per_sm, int(bool(force_vec)))
     _check(_lib.tp_tma_transpose_2d_ex(_ptr(src), _ptr(dst), rows, cols, ld_src, ld_dst, ctypes.byref(o),
                                        _stream(stream)), "tp_tma_transpose_2d_ex")
@@ -271,6 +292,8 @@ def tp_device_status(stream=None) -> int:
 
 
 def tp_device_status_detail(stream=None):
+    """Like tp_device_status, plus where the failure was recorded: (status, site, block,
+    thread)."""
     site, block, thread = _I(), _I(), _I()
     st = _lib.tp_device_status_detail(_stream(stream), ctypes.byref(site), ctypes.byref(block),
                                       ctypes.byref(thread))
@@ -294,12 +317,15 @@ def tp_gemm_plan(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, sm_count=0, **o
 
 
 def tp_last_plan() -> dict:
+    """The plan (path, variant, launch shape) of this thread's last GEMM / conv / copy call."""
     p = tp_plan()
     _check(_lib.tp_last_plan(ctypes.byref(p)), "tp_last_plan")
     return p.as_dict()
 
 
 def tp_list_kernels():
+    """Every compiled mainloop variant, as dicts (atom, pipe_depth, tile_n, out_f32, conv,
+    smem_bytes, ldg, splitk)."""
     n = _lib.tp_list_kernels(None, 0)
     arr = (tp_kernel_desc * n)()
     _lib.tp_list_kernels(arr, n)
@@ -315,11 +341,15 @@ def tp_probe_fma_latency(kind: int, chain: int = 65536, seed: float = 0.0, strea
 
 
 def tp_selftest_mainloop_withheld_arrival(A, B, C, M, N, K, limit_ms, stream=None):
+    """Runs the 1-SM mainloop with its first stage's arrival withheld, so that
+    its bounded waits must give up after `limit_ms`; the device status then reads TP_ERR_TIMEOUT."""
     _check(_lib.tp_selftest_mainloop_withheld_arrival(_ptr(A), _ptr(B), _ptr(C), M, N, K, limit_ms, _stream(stream)),
            "tp_selftest_mainloop_withheld_arrival")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None):
+    """Launches one bounded wait that nothing satisfies (`limit_us`); returns the device
+    status it leaves."""
     _check(_lib.tp_selftest_wait_timeout(limit_us, _stream(stream)), "tp_selftest_wait_timeout")
 
 
