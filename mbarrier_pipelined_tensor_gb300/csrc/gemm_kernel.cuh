@@ -353,6 +353,10 @@ __global__ void __launch_bounds__(192, 1)
                     // half-width units (2-SM, N = 256 only) load B through the half-height box
                     const bool hu = CG == 2 && BN == 256 && w.half >= 0;
                     const CUtensorMap* const mB = hu ? &mapBh : &mapB;
+                    // GEMM units of odd waves walk K backwards: the clusters
+                    // of one wave share A rows with the wave before, whose
+                    // last K blocks are the ones still in L2.
+                    [[maybe_unused]] const int kb_flip = (plt & 1) ? w.kb0 + w.kb1 - 1 : -1;
                     [[maybe_unused]] int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
                     if constexpr (CONV) {
                         const int pq = p.conv_P * p.conv_Q;
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(192, 1)
                                 }
                             }
                         } else {
-                            const int kx = kb * Cfg::BK;
+                            const int kx = (kb_flip < 0 ? kb : kb_flip - kb) * Cfg::BK;
                             if constexpr (CL) {
                                 if constexpr (HA) tma_load_2d_pair(dA, &mapA, fb, kx, m_row, pol_a);
                                 else tma_load_2d_pair(dA, &mapA, fb, kx, m_row);
