@@ -102,8 +102,8 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               throughput; the split-K entry points choose among N >= 128
  *               only.
  *   group_m:    tile raster: group_m M-tiles share one sweep over N
- *               (0 = 2048 rows of A per group: 16 tiles of the 1-SM atom,
- *               8 pair tiles of the 2-SM atom).
+ *               (0 = 3072 rows of A per group: 24 tiles of the 1-SM atom,
+ *               12 pair tiles of the 2-SM atom).
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM). A cap at
  *               or above the work-unit count (CTAs = units x atom; units =
  *               tiles, plus the narrow tail's extra halves) launches one
