@@ -229,6 +229,31 @@ def test_gemm_persistent_many_tiles_small_grid():
         check_against_oracle(got, ref, ab, True, f"persistent n{tile_n}")
 
 
+@pytest.mark.parametrize("atom,tile_n", [(1, 64), (1, 128), (1, 256), (2, 128), (2, 256)])
+def test_gemm_odd_waves_walk_k_backwards(atom, tile_n):
+    # A persistent CTA's odd-numbered units load their K blocks last to first.
+    # Two clusters over many tiles give every CTA several odd waves. With a
+    # permutation A every output is one product, exact in any order, so a K
+    # block loaded from the wrong coordinate shows as a wrong element.
+    M = K = 640
+    N = 384
+    perm = np.random.default_rng(17).permutation(K)
+    A = np.zeros((M, K), dtype=np.uint16)
+    A[np.arange(M), perm] = ONE
+    B = datagen.Stream(18).uniform_bf16((N, K))
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=atom, tile_n=tile_n, max_ctas=2 * atom,
+                         group_m=2, no_tail=1)
+    assert plan["grid"] == 2 * atom and plan["m_tiles"] * plan["n_tiles"] >= 6
+    assert np.array_equal(got, datagen.bf16_to_f32(B).astype(np.float64)[:, perm].T)
+    # Ragged K (the last block partly past K) on random operands, with the
+    # narrow tail on where the variant has one.
+    M, N, K = 700, 520, 1000
+    A, B = datagen.gemm_operands(M, N, K, seed=19)
+    got, plan = run_gemm(A, B, M, N, K, K, K, out_f32=True, atom=atom, tile_n=tile_n, max_ctas=4 * atom)
+    ref, ab = oracle.gemm(A, B, M, N, K, K, K)
+    check_against_oracle(got, ref, ab, True, f"odd waves atom{atom} n{tile_n}")
+
+
 # ---------------------------------------------- plain-load producer ---
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,ldc,offs", [

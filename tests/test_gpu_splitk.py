@@ -51,6 +51,19 @@ def test_splitk_every_variant_ragged(atom, tile_n):
     check_against_oracle(got, ref, ab, True, f"split-K atom{atom} n{tile_n}")
 
 
+@pytest.mark.parametrize("atom,tile_n", [(1, 128), (2, 256)])
+def test_splitk_odd_waves(atom, tile_n):
+    # Two clusters over 3 slices of every tile: most (tile, slice) units run
+    # in odd waves, whose K blocks are loaded last to first.
+    M, N, K = 300, 201, 1001
+    lda = ldb = 1008  # split-K feeds the mainloop through TMA: 16-byte pitches
+    A, B = datagen.gemm_operands(M, N, K, seed=64, lda=lda, ldb=ldb)
+    got, plan = run_splitk(A, B, M, N, K, lda, ldb, N, True, 3, atom=atom, tile_n=tile_n, max_ctas=2 * atom)
+    assert plan["splits"] == 3 and plan["grid"] == 2 * atom
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    check_against_oracle(got, ref, ab, True, f"split-K odd waves atom{atom} n{tile_n}")
+
+
 def test_splitk_slices_never_empty():
     # K = 130 is 3 K blocks; 5 slices asked -> 3 used, each non-empty.
     M, N, K = 256, 256, 136
