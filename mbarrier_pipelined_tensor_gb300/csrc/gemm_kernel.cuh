@@ -83,7 +83,10 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt,
     const int gm = min(p.m_tiles - first, p.group_m);
     const int r = t - g * group;
     mt = first + r % gm;
-    nt = r / gm;
+    // odd groups sweep N from the far end, starting on the B columns the
+    // group before ended on
+    const int n = r / gm;
+    nt = (g & 1) ? p.n_tiles - 1 - n : n;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits)
