@@ -79,6 +79,11 @@ enum {
  * The TMA producer needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2
  * multiples of 16; other layouts take the plain-load producer (1-SM atom,
  * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED).
+ * Repeating a call gives the same bits. The fp32 summation order of a tile
+ * depends on the variant and on the wave the tile runs in (a persistent
+ * CTA's odd-numbered tiles take their K blocks last to first), so calls
+ * whose options or grid differ may differ in rounding, within the same
+ * accumulator error bound.
  */
 TP_API int tp_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                  int64_t ldb, int64_t ldc, void* stream);
