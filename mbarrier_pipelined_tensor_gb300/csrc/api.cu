@@ -299,8 +299,6 @@ void normalize_splits(int64_t k_blocks, int* splits, int* kb_per_split)
     *splits = static_cast<int>(cdiv(k_blocks, kps));
 }
 
-
-
 int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom);
 
 // Narrow tail for the 2-SM atom at N = 256: when the tiles left for the last,
@@ -732,50 +730,50 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
     if (!ldg) {
-    Im2colDesc dx{};
-    dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    dx.base = const_cast<void*>(x);
-    dx.dims[0] = static_cast<uint64_t>(C);
-    dx.dims[1] = static_cast<uint64_t>(W);
-    dx.dims[2] = static_cast<uint64_t>(H);
-    dx.dims[3] = static_cast<uint64_t>(N);
-    dx.strides_bytes[0] = static_cast<uint64_t>(C) * 2;
-    dx.strides_bytes[1] = static_cast<uint64_t>(W * C) * 2;
-    dx.strides_bytes[2] = static_cast<uint64_t>(H * W * C) * 2;
-    // Bounding box of the filter window's first tap: from -pad to
-    // (extent - 1) + pad - (filter - 1), the positions output pixels start at.
-    dx.lower[0] = static_cast<int>(-pad);
-    dx.lower[1] = static_cast<int>(-pad);
-    dx.upper[0] = static_cast<int>(pad - (S - 1));
-    dx.upper[1] = static_cast<int>(pad - (R - 1));
-    dx.channels = 64;
-    dx.pixels = 128;
-    dx.elem_strides[0] = 1;
-    dx.elem_strides[1] = static_cast<uint32_t>(stride);
-    dx.elem_strides[2] = static_cast<uint32_t>(stride);
-    dx.elem_strides[3] = 1;
-    dx.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
-    if (dx.upper[0] < -128 || dx.upper[1] < -128) return TP_ERR_UNSUPPORTED;
-    TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w),
-                 {static_cast<uint64_t>(C), static_cast<uint64_t>(R * S), static_cast<uint64_t>(K)},
-                 {static_cast<uint64_t>(C) * 2, static_cast<uint64_t>(R * S * C) * 2},
-                 {64, 1, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
-    const uint32_t eb = out_f32 ? 4 : 2;
-    TiledDesc dy{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y,
-                 {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
-                 {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
-    if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw))) return st;
-    L.mapBh = L.mapB;
-    if (pl.atom == 2 && pl.tile_n == 256) {
-        TiledDesc dwh = dw;
-        dwh.box[2] = static_cast<uint32_t>(b_rows / 2);
-        if ((st = encode_tiled(&L.mapBh, dwh))) return st;
-    }
-    if (y_tma) {
-        if ((st = encode_tiled(&L.mapC, dy))) return st;
-    } else {
-        L.mapC = L.mapB;  // never stored through (n_tma = 0)
-    }
+        Im2colDesc dx{};
+        dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        dx.base = const_cast<void*>(x);
+        dx.dims[0] = static_cast<uint64_t>(C);
+        dx.dims[1] = static_cast<uint64_t>(W);
+        dx.dims[2] = static_cast<uint64_t>(H);
+        dx.dims[3] = static_cast<uint64_t>(N);
+        dx.strides_bytes[0] = static_cast<uint64_t>(C) * 2;
+        dx.strides_bytes[1] = static_cast<uint64_t>(W * C) * 2;
+        dx.strides_bytes[2] = static_cast<uint64_t>(H * W * C) * 2;
+        // Bounding box of the filter window's first tap: from -pad to
+        // (extent - 1) + pad - (filter - 1), the positions output pixels start at.
+        dx.lower[0] = static_cast<int>(-pad);
+        dx.lower[1] = static_cast<int>(-pad);
+        dx.upper[0] = static_cast<int>(pad - (S - 1));
+        dx.upper[1] = static_cast<int>(pad - (R - 1));
+        dx.channels = 64;
+        dx.pixels = 128;
+        dx.elem_strides[0] = 1;
+        dx.elem_strides[1] = static_cast<uint32_t>(stride);
+        dx.elem_strides[2] = static_cast<uint32_t>(stride);
+        dx.elem_strides[3] = 1;
+        dx.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+        if (dx.upper[0] < -128 || dx.upper[1] < -128) return TP_ERR_UNSUPPORTED;
+        TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w),
+                     {static_cast<uint64_t>(C), static_cast<uint64_t>(R * S), static_cast<uint64_t>(K)},
+                     {static_cast<uint64_t>(C) * 2, static_cast<uint64_t>(R * S * C) * 2},
+                     {64, 1, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
+        const uint32_t eb = out_f32 ? 4 : 2;
+        TiledDesc dy{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y,
+                     {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
+                     {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+        if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw))) return st;
+        L.mapBh = L.mapB;
+        if (pl.atom == 2 && pl.tile_n == 256) {
+            TiledDesc dwh = dw;
+            dwh.box[2] = static_cast<uint32_t>(b_rows / 2);
+            if ((st = encode_tiled(&L.mapBh, dwh))) return st;
+        }
+        if (y_tma) {
+            if ((st = encode_tiled(&L.mapC, dy))) return st;
+        } else {
+            L.mapC = L.mapB;  // never stored through (n_tma = 0)
+        }
     }
     GemmParams& p = L.params;
     p.A = static_cast<const uint16_t*>(x);

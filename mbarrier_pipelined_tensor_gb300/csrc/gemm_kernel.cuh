@@ -192,8 +192,6 @@ __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& 
     return w;
 }
 
-
-
 // Role timeline: adds `v` to this CTA's counter `slot` when tracing is on.
 __device__ __forceinline__ void trace_add(const GemmParams& p, int slot, unsigned long long v)
 {
