@@ -430,7 +430,9 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
     rows["tma_transpose_1GiB"] = {"unit": "GB/s", "gbs": round(gbs, 1),
                                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3), "ms": round(ms, 4),
                                   "bit_exact": bool(torch.equal(dst, src.t()))}
-    del src, dst
+    del dst
+    rows["fallback_paths"] = fallback_paths(torch, tp, stream, src, peaks)
+    del src
 
     # dependent fma chains (RAW latency upper bound, SM cycles per link)
     probe = {}
@@ -440,6 +442,54 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
     probe["pages_b200"] = {"ffma_f32": 4, "dfma_f64": 8}
     rows["fma_chain_latency"] = probe
     return rows
+
+
+def fallback_paths(torch, tp, stream, src, peaks):
+    """The paths taken where TMA cannot describe the operands: the
+    vectorized copy and tile transpose (forced on the same 1 GiB matrix), and
+    the plain-load producer feeding the tcgen05 mainloop (a 4096^3 GEMM whose
+    odd pitches rule TMA out), next to the TMA producer on the same shape."""
+    s = stream.cuda_stream
+    rr, cc = src.shape
+    moved = 2.0 * rr * cc * 2
+    out = {}
+    dst = torch.empty_like(src)
+    cp = lambda: tp.tp_tma_copy_2d_ex(src, dst, rr, cc, cc, stream=s, force_vec=True)  # noqa: E731
+    for _ in range(3):
+        cp()
+    ms = time_loop(torch, stream, cp, 20) / 20
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_COPY
+    out["vec_copy_1GiB"] = {"unit": "GB/s", "gbs": round(moved / (ms * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                            "bit_exact": bool(torch.equal(src, dst))}
+    del dst
+    dst = torch.empty((cc, rr), dtype=torch.int16, device="cuda")
+    tr = lambda: tp.tp_tma_transpose_2d_ex(src, dst, rr, cc, cc, rr, stream=s, force_vec=True)  # noqa: E731
+    for _ in range(3):
+        tr()
+    ms = time_loop(torch, stream, tr, 20) / 20
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_TRANSPOSE
+    out["vec_transpose_1GiB"] = {"unit": "GB/s", "gbs": round(moved / (ms * 1e-3) / 1e9, 1),
+                                 "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                                 "bit_exact": bool(torch.equal(dst, src.t()))}
+    del dst
+    M = N = K = 4096
+    flops = 2.0 * M * N * K
+    gen = torch.Generator(device="cuda").manual_seed(7)
+    for name, ld in (("plain_load_producer_4096", K + 1), ("tma_producer_4096_same_variant", K)):
+        a = (torch.randn(M * ld, device="cuda", generator=gen) * 0.02).bfloat16()
+        b = (torch.randn(N * ld, device="cuda", generator=gen) * 0.02).bfloat16()
+        c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        g = lambda: tp.tp_gemm_bf16_ex(a, b, c, M, N, K, ld, ld, N, stream=s, atom=1, tile_n=128)  # noqa: E731
+        for _ in range(3):
+            g()
+        ms = time_loop(torch, stream, g, 20) / 20
+        plan = tp.tp_last_plan()
+        out[name] = {"unit": "TFLOP/s", "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "lda": ld,
+                     "path": "plain-load" if plan["path"] == tp.TP_PATH_FALLBACK_MAINLOOP else "tma",
+                     "atom": plan["atom"], "tile_n": plan["tile_n"], "pipe_depth": plan["pipe_depth"]}
+        del a, b, c
+    return out
 
 
 def library_comparison(torch, stream, flush_buf, headline_step):
