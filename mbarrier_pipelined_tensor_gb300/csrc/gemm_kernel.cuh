@@ -103,24 +103,32 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // 8 consecutive bf16 (one 16-byte chunk of a swizzle row) gathered with
 // bounds checks; out-of-range elements are zero, as TMA's fill would be.
+// row_ptr must point at a readable row even when row_ok is false. Every load
+// is issued unconditionally, from element 0 of that row when its own element
+// is out of range, so the loads of several chunks can be in flight at once.
 __device__ __forceinline__ void gather8(const uint16_t* __restrict__ row_ptr, bool row_ok, int col0, int cols,
                                         uint32_t (&v)[4])
 {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int c = col0 + 2 * e;
-        const uint32_t lo = (row_ok && c < cols) ? row_ptr[c] : 0u;
-        const uint32_t hi = (row_ok && c + 1 < cols) ? row_ptr[c + 1] : 0u;
-        v[e] = lo | (hi << 16);
+        const bool lo_ok = row_ok && c < cols;
+        const bool hi_ok = row_ok && c + 1 < cols;
+        const uint32_t lo = __ldg(row_ptr + (lo_ok ? c : 0));
+        const uint32_t hi = __ldg(row_ptr + (hi_ok ? c + 1 : 0));
+        v[e] = (lo_ok ? lo : 0u) | ((hi_ok ? hi : 0u) << 16);
     }
 }
 
 // Fills one stage (A: 128 rows, B: B_ROWS rows, 64 bf16 each) with plain
-// loads; lane L handles chunks L, L+32, ... (8 chunks per 128-byte row).
+// loads; lane L handles chunks L, L+32, ... (8 chunks per 128-byte row). The
+// loads of kBatch chunks per lane are issued before any of them is stored.
 template <int B_ROWS, bool CONV>
 __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA, uint32_t dB, int m_row, int n_row,
                                                int kb, uint32_t lane)
 {
+    constexpr int kBatch = 8;
+    static_assert((128 * 8) % (32 * kBatch) == 0 && (B_ROWS * 8) % (32 * kBatch) == 0, "whole batches");
     int r = 0, sx = 0, c0 = kb * 64;
     if constexpr (CONV) {
         const int rs = kb / p.conv_cblocks;
@@ -128,10 +136,9 @@ __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA,
         r = rs / p.conv_S;
         sx = rs - r * p.conv_S;
     }
-    for (int idx = static_cast<int>(lane); idx < 128 * 8; idx += 32) {
+    auto load_a = [&](int idx, uint32_t (&v)[4]) {
         const int row = idx >> 3, j = idx & 7;
         const int m = m_row + row;
-        uint32_t v[4];
         if constexpr (CONV) {
             const int pq = p.conv_P * p.conv_Q;
             const int img = m / pq;
@@ -141,20 +148,19 @@ __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA,
             const int h = pp * p.conv_stride - p.conv_pad + r;
             const int w = qq * p.conv_stride - p.conv_pad + sx;
             const bool ok = m < p.M && h >= 0 && h < p.conv_H && w >= 0 && w < p.conv_W;
-            const uint16_t* rp = p.A + ((static_cast<int64_t>(img) * p.conv_H + (ok ? h : 0)) * p.conv_W +
-                                        (ok ? w : 0)) * p.conv_C;
+            // an out-of-range pixel reads (harmlessly) the first input row
+            const uint16_t* rp =
+                ok ? p.A + ((static_cast<int64_t>(img) * p.conv_H + h) * p.conv_W + w) * p.conv_C : p.A;
             gather8(rp, ok, c0 + j * 8, p.conv_C, v);
         } else {
             const bool ok = m < p.M;
             gather8(p.A + static_cast<int64_t>(ok ? m : 0) * p.lda, ok, c0 + j * 8, p.K, v);
         }
-        st_shared_v4(dA + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
-    }
-    for (int idx = static_cast<int>(lane); idx < B_ROWS * 8; idx += 32) {
+    };
+    auto load_b = [&](int idx, uint32_t (&v)[4]) {
         const int row = idx >> 3, j = idx & 7;
         const int n = n_row + row;
         const bool ok = n < p.N;
-        uint32_t v[4];
         if constexpr (CONV) {
             const uint16_t* rp =
                 p.B + ((static_cast<int64_t>(ok ? n : 0) * p.conv_R + r) * p.conv_S + sx) * p.conv_C;
@@ -162,7 +168,27 @@ __device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA,
         } else {
             gather8(p.B + static_cast<int64_t>(ok ? n : 0) * p.ldb, ok, c0 + j * 8, p.K, v);
         }
-        st_shared_v4(dB + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
+    };
+    auto store = [&](uint32_t dst, int idx, const uint32_t (&v)[4]) {
+        const int row = idx >> 3, j = idx & 7;
+        st_shared_v4(dst + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
+    };
+    const int li = static_cast<int>(lane);
+#pragma unroll 1
+    for (int base = 0; base < 128 * 8; base += 32 * kBatch) {
+        uint32_t v[kBatch][4];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) load_a(base + i * 32 + li, v[i]);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) store(dA, base + i * 32 + li, v[i]);
+    }
+#pragma unroll 1
+    for (int base = 0; base < B_ROWS * 8; base += 32 * kBatch) {
+        uint32_t v[kBatch][4];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) load_b(base + i * 32 + li, v[i]);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) store(dB, base + i * 32 + li, v[i]);
     }
 }
 
