@@ -78,7 +78,8 @@ enum {
  *      (no alpha/beta). K == 0 writes zeros.
  * The TMA producer needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2
  * multiples of 16; other layouts take the plain-load producer (1-SM atom,
- * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED).
+ * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED),
+ * which is correct but about 50x slower on a large GEMM.
  * Repeating a call gives the same bits. The fp32 summation order of a tile
  * depends on the variant and on the wave the tile runs in (a persistent
  * CTA's odd-numbered tiles take their K blocks last to first), so calls
