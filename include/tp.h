@@ -5,8 +5,9 @@
  *
  * Conventions for every entry point:
  *  - Pointers are caller-owned DEVICE memory (any allocator). The library
- *    allocates no device memory; its only state is a static device status
- *    record per GPU and a cached driver entry point.
+ *    allocates no device memory; its state is a static device status
+ *    record per GPU, the static split-K array behind
+ *    tp_gemm_bf16_splitk_noalloc, and a cached driver entry point.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream). Calls are asynchronous on it; they return after the launch.
  *  - The return value reports what the host can see: invalid arguments, a
