@@ -223,8 +223,14 @@ TP_API int tp_gemm_splitk_workspace_bytes(int64_t M, int64_t N, int splits, int6
  *  - The partial sums live in a fixed 32 MiB array inside the library
  *    (tp_gemm_splitk_noalloc_capacity()); every GPU that loads the library
  *    holds it until the process exits. Nothing is allocated per call.
- *  - The first call on a device looks up the array's device address for
- *    that device; make that first call before any stream capture.
+ *  - The array is created on a device when the library's module first loads
+ *    there, which CUDA's lazy loading puts at the library's first call of
+ *    any kind on that device. A caller that must not allocate later makes
+ *    one library call per device during its set-up (tp_device_status, for
+ *    example), so that the creation happens then.
+ *  - The first call of this entry point on a device looks up the array's
+ *    device address for that device; make that first call before any
+ *    stream capture.
  *  - An explicit `splits` whose workspace (tp_gemm_splitk_workspace_bytes)
  *    exceeds the array returns TP_ERR_WORKSPACE_LIMIT; splits = 0 chooses
  *    only counts that fit (one slice needs no workspace).

@@ -67,6 +67,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose:
             print(os.path.basename(src), "ok", flush=True)
 
+    # Objects of sources that no longer exist are removed: they are never
+    # linked, and nothing stale should travel with the tree.
+    live = {obj_of(s) for s in srcs}
+    for o in glob.glob(os.path.join(BUILD, "*.o")):
+        if o not in live:
+            os.remove(o)
     todo = [s for s in srcs if needs(s)]
     if todo:
         with ThreadPoolExecutor(max(1, min(len(todo), os.cpu_count() or 1))) as ex:

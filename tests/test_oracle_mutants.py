@@ -44,3 +44,68 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# Mistakes in the acceptance rule (oracle/__init__.py), planted in a copy of
+# the package that the pin suite then imports in place of the real one.
+TOLERANCE_MUTANTS = {
+    "bf16_term_2_pow_7": ("np.abs(ref) * 2.0 ** -8", "np.abs(ref) * 2.0 ** -7"),
+    "bf16_term_2_pow_9": ("np.abs(ref) * 2.0 ** -8", "np.abs(ref) * 2.0 ** -9"),
+    "bf16_term_signed": ("np.abs(ref) * 2.0 ** -8", "ref * 2.0 ** -8"),
+    "bf16_term_on_fp32": ("    if out_bf16:\n        tol = tol + np.abs(ref)", "    if True:\n        tol = tol + np.abs(ref)"),
+    "abs_scale_1e_2": ("tol = 1e-3 * ab + 1e-6", "tol = 1e-2 * ab + 1e-6"),
+}
+
+_LOAD_MUTANT = """
+import importlib.util, sys
+pkg = sys.argv[1]
+spec = importlib.util.spec_from_file_location("oracle", pkg + "/__init__.py", submodule_search_locations=[pkg])
+mod = importlib.util.module_from_spec(spec)
+sys.modules["oracle"] = mod
+spec.loader.exec_module(mod)
+import pytest
+sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", sys.argv[2]]))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(TOLERANCE_MUTANTS))
+def test_pins_catch_planted_tolerance_mistake(name, tmp_path):
+    import shutil
+
+    sys.path.insert(0, ROOT)
+    from oracle import build as oracle_build
+
+    lib = oracle_build.build()
+    old, new = TOLERANCE_MUTANTS[name]
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    for f in ("__init__.py", "build.py", "oracle.c"):
+        shutil.copy(os.path.join(ROOT, "oracle", f), pkg / f)
+    src = (pkg / "__init__.py").read_text()
+    assert src.count(old) == 1, "mutation anchor not found"
+    (pkg / "__init__.py").write_text(src.replace(old, new, 1))
+    env = dict(os.environ, ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-c", _LOAD_MUTANT, str(pkg),
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+
+
+def test_unmutated_copy_passes_the_pins(tmp_path):
+    # The loader above runs the real acceptance rule cleanly, so a failing
+    # mutant run means its planted mistake, not the harness.
+    import shutil
+
+    sys.path.insert(0, ROOT)
+    from oracle import build as oracle_build
+
+    lib = oracle_build.build()
+    pkg = tmp_path / "oracle"
+    pkg.mkdir()
+    for f in ("__init__.py", "build.py", "oracle.c"):
+        shutil.copy(os.path.join(ROOT, "oracle", f), pkg / f)
+    env = dict(os.environ, ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-c", _LOAD_MUTANT, str(pkg),
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:]

@@ -182,6 +182,60 @@ def test_acceptance_rule():
     assert not ok
 
 
+# bf16 outputs. ref = +-3 with sum|a*b| = 5: the fp32 bound is
+# 1e-3 * 5 + 1e-6 = 0.005001 and half a bf16 ulp of the true value adds
+# 2**-8 * 3 = 0.01171875, so the bf16 bound is 0.01671975 on either sign.
+# A term of 2**-7 (0.0284385), a signed ref (0.005001 - 0.01171875 < 0 for
+# ref = -3) or the term on fp32 outputs (0.01671975) each flips one of the
+# accept / reject decisions below.
+@pytest.mark.parametrize("ref", [3.0, -3.0])
+def test_acceptance_bf16_bound_edges(ref):
+    r = np.array([ref])
+    ab = np.array([5.0])
+    for sign in (1.0, -1.0):
+        ok, _, _ = oracle.check(r + sign * 0.01671, r, ab, out_bf16=True)
+        assert ok, f"ref {ref}: error 0.01671 is inside the bf16 bound 0.01671975"
+        ok, _, nbad = oracle.check(r + sign * 0.01673, r, ab, out_bf16=True)
+        assert not ok and nbad == 1, f"ref {ref}: error 0.01673 is outside the bf16 bound"
+
+
+def test_acceptance_fp32_has_no_bf16_term():
+    r = np.array([3.0, -3.0])
+    ab = np.array([5.0, 5.0])
+    ok, _, _ = oracle.check(r + 0.00500, r, ab, out_bf16=False)
+    assert ok
+    ok, _, nbad = oracle.check(r + np.array([0.00501, -0.00501]), r, ab, out_bf16=False)
+    assert not ok and nbad == 2, "fp32 bound is 0.005001: no half-ulp term"
+
+
+def test_acceptance_bf16_admits_rounding_of_a_close_fp32_result():
+    # True value 1 + 2**-8 + 2**-20 (one product, so sum|a*b| = the value).
+    # An fp32 result one ulp (2**-23) above it rounds (RNE) to the bf16
+    # value 1 + 2**-7, an error of 2**-8 - 2**-20 - 2**-23 = 0.00390506;
+    # the bf16 bound, 1e-3 * v + 1e-6 + 2**-8 * v = 0.00492646, admits it,
+    # the fp32 bound (0.00100491) does not.
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -20
+    near = np.array([v + 2.0 ** -23], dtype=np.float32)
+    rounded = datagen.bf16_to_f32(datagen.f32_to_bf16_rne(near)).astype(np.float64)
+    assert rounded[0] == 1.0 + 2.0 ** -7
+    r, ab = np.array([v]), np.array([v])
+    ok, _, _ = oracle.check(rounded, r, ab, out_bf16=True)
+    assert ok
+    ok, _, _ = oracle.check(rounded, r, ab, out_bf16=False)
+    assert not ok
+
+
+def test_acceptance_bf16_admits_a_tie_rounded_to_even():
+    # 1 + 2**-8 lies halfway between the bf16 values 1 and 1 + 2**-7 and
+    # rounds to the even one, 1: an error of exactly half an ulp (2**-8).
+    # With a quarter-ulp term (2**-9 * v) the bound would be 0.00296794.
+    v = 1.0 + 2.0 ** -8
+    rounded = datagen.bf16_to_f32(datagen.f32_to_bf16_rne(np.array([v], dtype=np.float32)))
+    assert rounded[0] == 1.0
+    ok, worst, _ = oracle.check(rounded.astype(np.float64), np.array([v]), np.array([v]), out_bf16=True)
+    assert ok and worst > 0.75, "a half-ulp error uses most of the bf16 bound"
+
+
 # ----------------------------------------------------------------- conv -----
 
 def conv_ref(x, w, N, H, W, C, K, R, S, st, pad):
