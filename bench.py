@@ -9,7 +9,9 @@ The same run also measures the other rows of the path, each against its
 roofline: the implicit-GEMM conv (32x56x56x256, 3x3, K 256), the 1 GiB TMA
 copy (GB/s vs HBM), the skinny GEMM set and the small ragged GEMM.
 
-One JSON line on stdout (rank 0). Multi-GPU (torchrun): every rank runs the
+Two JSON lines on stdout (rank 0): the full per-row record
+({"bench_detail": ...}), then the bench line, which ends with a compact
+per-row "summary". Multi-GPU (torchrun): every rank runs the
 same problem on its own GPU (replicas: the path has no cross-GPU exchange);
 value = all ranks' FLOPs / the slowest rank's time.
 
@@ -46,7 +48,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["tp", "reference"], default="tp")
     ap.add_argument("--no-rows", action="store_true", help="only the headline GEMM")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--sweep", action="store_true", help="also run the PIPE_DEPTH x atom sweep")
+    ap.add_argument("--sweep", action="store_true", help="(kept for old command lines: the PIPE_DEPTH x atom sweep "
+                    "runs with the rows)")
     ap.add_argument("--atom", type=int, default=0)
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--depth", type=int, default=0)
@@ -635,6 +638,54 @@ def row_oracle_timings(rows):
     return out
 
 
+def summarize(value, achieved, peak, rows, sweep, peaks):
+    """Compact per-row results for the end of the bench line: value, unit,
+    fraction of its bound and the same-run vendor-library figure."""
+    out = {"gemm_8192x8192x8192": {"tflops": round(value, 1), "frac": round(achieved / peak, 3)}}
+    lib = (rows or {}).get("library_comparison", {})
+    if "gemm_8192x8192x8192" in lib:
+        out["gemm_8192x8192x8192"]["cublas_tflops"] = lib["gemm_8192x8192x8192"]["tflops"]
+    if rows:
+        cv = rows.get("conv_32x56x56x256_3x3", {})
+        if "auto" in cv:
+            a = cv["auto"]
+            out["conv_32x56x56x256_3x3"] = {
+                "tflops": a["tflops"], "us": a["us"], "frac": a["frac_of_peak"],
+                "variant": f"{a['atom']}/{a['tile_n']}/{a['pipe_depth']}",
+                "cudnn_tflops": lib.get("conv_32x56x56x256_3x3", {}).get("tflops")}
+        for key, r in rows.get("skinny_gemm_set", {}).items():
+            if not isinstance(r, dict) or "tflops" not in r:
+                continue
+            e = {"tflops": r["tflops"], "us": r["us"], "frac": r["frac"], "bound_tflops": r["roofline_tflops"],
+                 "cublas_tflops": lib.get(f"gemm_{key}", {}).get("tflops")}
+            sk = r.get("splitk")
+            if sk and sk.get("splits", 1) > 1:
+                e["splitk_tflops"] = sk["tflops"]
+                e["splitk_frac"] = sk["frac"]
+                e["splits"] = sk["splits"]
+            out[f"gemm_{key}"] = e
+        sm = rows.get("gemm_320x200x448_f32")
+        if sm:
+            out["gemm_320x200x448_f32"] = {"us": sm["median_us"],
+                                           "cublas_us": lib.get("gemm_320x200x448", {}).get("us")}
+        for key, lk in (("tma_copy_1GiB", "copy_1GiB"), ("tma_transpose_1GiB", "transpose_1GiB")):
+            r = rows.get(key)
+            if r:
+                out[key] = {"gbs": r["gbs"], "frac": r["frac_of_hbm"], "bit_exact": r["bit_exact"],
+                            "torch_gbs": lib.get(lk, {}).get("gbs")}
+        fb = rows.get("fallback_paths", {})
+        if "plain_load_producer_4096" in fb:
+            out["plain_load_producer_4096"] = {"tflops": fb["plain_load_producer_4096"]["tflops"],
+                                               "tma_tflops": fb["tma_producer_4096_same_variant"]["tflops"]}
+    if sweep:
+        sw = {}
+        for r in sweep:
+            sw.setdefault(f"{r['atom']}/{r['tile_n']}", []).append(r.get("tflops"))
+        out["depth_sweep_tflops"] = {"depths_from": 2, **sw}
+    out["peaks"] = {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"]}
+    return out
+
+
 # ----------------------------------------------------------------- arms ---
 
 def reference_arm(args):
@@ -813,7 +864,7 @@ def tp_arm(args):
         rows = measure_rows(torch, tp, stream, peaks, flush_buf)
         rows["library_comparison"] = library_comparison(torch, stream, flush_buf, step)
         del flush_buf
-    if rank == 0 and args.sweep:
+    if rank == 0 and not args.no_rows and args.size == 8192:
         sweep = run_sweep(torch, tp, stream, a, b, c, M, N, K, peaks)
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(M, N, K, A, B)
@@ -851,10 +902,13 @@ def tp_arm(args):
             "clocks": clocks,
             "gpu_launches": args.steps,
             "role_timeline": timeline,
-            "rows": rows,
+            # Last, so that the tail of stdout always shows every row.
+            "summary": summarize(value, achieved, peak, rows, sweep, peaks),
         }
-        if sweep is not None:
-            line["sweep"] = sweep
+        # The full per-row record (role timelines, oracle timings, library
+        # figures, the fallback paths) on a line of its own before the
+        # bench line.
+        print(json.dumps({"bench_detail": {"rows": rows, "sweep": sweep}}), flush=True)
         print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
