@@ -141,6 +141,9 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *   events:     NULL, or a caller-owned, zeroed device buffer of
  *               TP_EVENT_SLOTS x (CTAs of the launch) uint64: the per-unit
  *               event timeline below. Both buffers may be given at once.
+ *   protocol:   NULL, or a caller-owned, zeroed device buffer of
+ *               TP_PROTO_SLOTS x (CTAs of the launch) uint32: the arrival
+ *               accounting below (GEMM without split-K, and conv).
  * A (atom, depth, tile_n) whose stages do not fit the 232,448-byte shared
  * memory of a CTA returns TP_ERR_SMEM_BUDGET, the analogue of the note's
  * "StageCount<9> fails the capacity assert"; a combination that fits but is
@@ -156,7 +159,33 @@ typedef struct {
     int no_tail;
     uint64_t* trace;
     uint64_t* events;
+    uint32_t* protocol;
 } tp_gemm_opts;
+
+/* Arrival accounting per CTA (tp_gemm_opts.protocol), TP_PROTO_SLOTS uint32
+ * counters, for checking the stage ring's protocol on the device ("B200 Tma
+ * Pipeline Designer", step 8: each ready / free barrier has one producer and
+ * one consumer). Phase k of a barrier is the k-th use of its stage or
+ * accumulator; counters of phases past TP_PROTO_PHASES - 1 add to the last.
+ *   [bar * TP_PROTO_PHASES + k]  arrivals issued on barrier `bar` in phase k:
+ *     bar = s (full[s]), TP_PROTO_MAX_STAGES + s (empty[s]),
+ *     2 * TP_PROTO_MAX_STAGES + b (acc_full[b]),
+ *     2 * TP_PROTO_MAX_STAGES + 2 + b (acc_empty[b]).
+ *   [TP_PROTO_TX_EXPECT + s * TP_PROTO_PHASES + k]  bytes full[s] was told to
+ *     expect (arrive.expect_tx) in phase k;
+ *   [TP_PROTO_TX_ISSUED + s * TP_PROTO_PHASES + k]  bytes of the TMA loads
+ *     issued into it (both CTAs of a pair).
+ * Counts sit on the CTA that owns the barrier: a 2-SM pair's full and
+ * acc_empty barriers are its leader's (even CTA); its MMA commits arrive on
+ * both CTAs' empty and acc_full barriers. The plain-load producer arrives on
+ * full[s] without transaction bytes. A counted launch runs an instrumented
+ * copy of the producer and MMA loops (one atomic per arrival). */
+#define TP_PROTO_MAX_STAGES 9
+#define TP_PROTO_PHASES 64
+#define TP_PROTO_BARS (2 * TP_PROTO_MAX_STAGES + 4)
+#define TP_PROTO_TX_EXPECT (TP_PROTO_BARS * TP_PROTO_PHASES)
+#define TP_PROTO_TX_ISSUED (TP_PROTO_TX_EXPECT + TP_PROTO_MAX_STAGES * TP_PROTO_PHASES)
+#define TP_PROTO_SLOTS (TP_PROTO_TX_ISSUED + TP_PROTO_MAX_STAGES * TP_PROTO_PHASES)
 
 /* Role-timeline counters per CTA (tp_gemm_opts.trace), in this order:
  * producer span, producer waiting for a free stage, MMA issuer span, MMA
@@ -432,6 +461,25 @@ TP_API int tp_probe_fma_latency(int kind, int chain, double seed, double* result
  */
 TP_API int tp_selftest_mainloop_withheld_arrival(const void* A, const void* B, float* C, int64_t M, int64_t N,
                                                  int64_t K, uint32_t limit_ms, void* stream);
+
+/*
+ * The other half of the lost-completion self test: the MMA issuer skips one
+ * tcgen05.commit, the failure "consuming right after the load is issued,
+ * missing the barrier wait" seen from the consumer's side ("B200 Tma Pipeline
+ * Designer", Failure modes). which = 1 skips the commit to empty[s] after its
+ * first k-block, so the producer's bounded wait for that stage (and the MMA
+ * issuer's wait for its refill) must give up (site 1 producer or 2 MMA
+ * issuer); which = 2 skips the commit to acc_full[b] after its first tile,
+ * so the epilogue's wait (site 4), and an MMA issuer's wait for that
+ * accumulator (site 3), must give up. The GEMM is C = A.B (fp32 C, lda =
+ * ldb = K, ldc = N) on atom 1 or 2 at MMA N = 128, each CTA's waits limited
+ * to limit_ms (1..10000); the kernel drains its MMAs and loads, frees tensor
+ * memory and returns, and tp_device_status reports TP_ERR_TIMEOUT. C is left
+ * unspecified. Sizes: M, N <= 4096, 64 <= K <= 4096; which = 1 needs more
+ * k-blocks (K / 64) than stages to reach a stage's second use.
+ */
+TP_API int tp_selftest_mainloop_skipped_commit(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                                               int64_t K, int which, int atom, uint32_t limit_ms, void* stream);
 
 /* Launches one CTA that waits on an mbarrier nothing arrives on, with a
  * limit of limit_us microseconds: the wait must give up and record

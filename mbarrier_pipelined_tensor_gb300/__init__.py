@@ -46,7 +46,8 @@ TP_PATH_VEC_TRANSPOSE = 7
 class tp_gemm_opts(ctypes.Structure):
     _fields_ = [("atom", ctypes.c_int), ("pipe_depth", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("group_m", ctypes.c_int), ("max_ctas", ctypes.c_int), ("l2_hint", ctypes.c_int),
-                ("no_tail", ctypes.c_int), ("trace", ctypes.c_void_p), ("events", ctypes.c_void_p)]
+                ("no_tail", ctypes.c_int), ("trace", ctypes.c_void_p), ("events", ctypes.c_void_p),
+                ("protocol", ctypes.c_void_p)]
 
 
 class tp_copy_opts(ctypes.Structure):
@@ -102,6 +103,7 @@ _SIGS = {
     "tp_list_kernels": ([ctypes.POINTER(tp_kernel_desc), _I], _I),
     "tp_selftest_wait_timeout": ([ctypes.c_uint32, _P], _I),
     "tp_selftest_mainloop_withheld_arrival": ([_P, _P, _P, _I64, _I64, _I64, ctypes.c_uint32, _P], _I),
+    "tp_selftest_mainloop_skipped_commit": ([_P, _P, _P, _I64, _I64, _I64, _I, _I, ctypes.c_uint32, _P], _I),
     "tp_probe_fma_latency": ([_I, _I, ctypes.c_double, ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(ctypes.c_double), _P], _I),
 }
@@ -178,6 +180,12 @@ def tp_gemm_bf16_f32(A, B, C, M, N, K, lda, ldb, ldc, stream=None):
 TRACE_SLOTS = 8
 TRACE_NAMES = ("producer_span", "producer_wait_empty", "mma_span", "mma_wait_full", "mma_wait_acc_empty",
                "epilogue_span", "epilogue_wait_acc_full", "units")
+PROTO_MAX_STAGES = 9
+PROTO_PHASES = 64
+PROTO_BARS = 2 * PROTO_MAX_STAGES + 4
+PROTO_TX_EXPECT = PROTO_BARS * PROTO_PHASES
+PROTO_TX_ISSUED = PROTO_TX_EXPECT + PROTO_MAX_STAGES * PROTO_PHASES
+PROTO_SLOTS = PROTO_TX_ISSUED + PROTO_MAX_STAGES * PROTO_PHASES
 EVENTS_PER_UNIT = 8
 EVENT_UNITS = 8
 EVENT_SLOTS = EVENTS_PER_UNIT * EVENT_UNITS
@@ -185,9 +193,10 @@ EVENT_NAMES = ("producer_start", "producer_end", "mma_start", "mma_end", "epilog
                "epilogue_stored", "unit")
 
 
-def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_tail=0, trace=None, events=None):
+def _opts(atom=0, pipe_depth=0, tile_n=0, group_m=0, max_ctas=0, l2_hint=0, no_tail=0, trace=None, events=None,
+          protocol=None):
     return tp_gemm_opts(atom, pipe_depth, tile_n, group_m, max_ctas, l2_hint, int(bool(no_tail)), _ptr(trace),
-                        _ptr(events))
+                        _ptr(events), _ptr(protocol))
 
 
 def tp_gemm_bf16_ex(A, B, C, M, N, K, lda, ldb, ldc, out_f32=False, stream=None, **opts):
@@ -345,6 +354,15 @@ def tp_selftest_mainloop_withheld_arrival(A, B, C, M, N, K, limit_ms, stream=Non
     its bounded waits must give up after `limit_ms`; the device status then reads TP_ERR_TIMEOUT."""
     _check(_lib.tp_selftest_mainloop_withheld_arrival(_ptr(A), _ptr(B), _ptr(C), M, N, K, limit_ms, _stream(stream)),
            "tp_selftest_mainloop_withheld_arrival")
+
+
+def tp_selftest_mainloop_skipped_commit(A, B, C, M, N, K, which, atom, limit_ms, stream=None):
+    """Runs the mainloop (atom 1 or 2, MMA N 128) with the MMA issuer skipping its first commit
+    to empty[s] (which = 1) or to acc_full[b] (which = 2), so that the waits behind it must give
+    up after `limit_ms`; the device status then reads TP_ERR_TIMEOUT."""
+    _check(_lib.tp_selftest_mainloop_skipped_commit(_ptr(A), _ptr(B), _ptr(C), M, N, K, which, atom, limit_ms,
+                                                    _stream(stream)),
+           "tp_selftest_mainloop_skipped_commit")
 
 
 def tp_selftest_wait_timeout(limit_us: int, stream=None):

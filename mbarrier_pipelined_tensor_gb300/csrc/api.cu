@@ -16,6 +16,10 @@
 
 static_assert(TP_TRACE_SLOTS == tp::kTraceSlots, "trace layout");
 static_assert(TP_EVENT_SLOTS == tp::kEventSlots && TP_EVENTS_PER_UNIT == tp::kEventsPerUnit, "event layout");
+static_assert(TP_PROTO_SLOTS == tp::kProtoSlots && TP_PROTO_PHASES == tp::PROTO_PHASES &&
+                  TP_PROTO_MAX_STAGES == tp::PROTO_MAX_STAGES && TP_PROTO_TX_EXPECT == tp::PROTO_TX_EXPECT &&
+                  TP_PROTO_TX_ISSUED == tp::PROTO_TX_ISSUED,
+              "arrival accounting layout");
 
 namespace tp {
 const KernelEntry* table_mainloop_cg1(int* n);
@@ -59,8 +63,10 @@ struct DeviceState {
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 thread_local int t_last_cuda_error = 0;
-// Set only inside tp_selftest_mainloop_withheld_arrival for its one launch.
+// Set only inside tp_selftest_mainloop_withheld_arrival /
+// tp_selftest_mainloop_skipped_commit for their one launch.
 thread_local int t_selftest_withhold = 0;
+thread_local int t_selftest_skip_commit = 0;
 thread_local uint64_t t_selftest_limit_ns = 0;
 thread_local tp_plan t_last_plan = {};
 
@@ -628,6 +634,8 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.ldc_bytes = use_splitk ? ldw * 4 : ldc * eb;
     p.wait = WaitCtl{dev->status, t_selftest_limit_ns ? t_selftest_limit_ns : wait_limit_ns()};
     p.withhold_first_arrival = t_selftest_withhold;
+    p.skip_commit = t_selftest_skip_commit;
+    p.proto = opts ? opts->protocol : nullptr;
     if (use_splitk) {
         const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
         L.grid = pl.grid;
@@ -803,6 +811,7 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.n_tma = (ldg || !y_tma) ? 0 : static_cast<int>(K);  // TMA stores: rows are whole 16-byte granules
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.events = opts ? reinterpret_cast<unsigned long long*>(opts->events) : nullptr;
+    p.proto = opts ? opts->protocol : nullptr;
     p.C = y;
     p.ldc_bytes = K * eb_out;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};
@@ -1027,6 +1036,23 @@ int tp_selftest_mainloop_withheld_arrival(const void* A, const void* B, float* C
     t_selftest_limit_ns = static_cast<uint64_t>(limit_ms) * 1000000ull;
     const int st = gemm_impl(A, B, C, M, N, K, K, K, N, 1, &o, 0, 0, nullptr, 0, stream);
     t_selftest_withhold = 0;
+    t_selftest_limit_ns = 0;
+    return st;
+}
+
+int tp_selftest_mainloop_skipped_commit(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                                        int which, int atom, uint32_t limit_ms, void* stream)
+{
+    if (limit_ms == 0 || limit_ms > 10000 || M > 4096 || N > 4096 || K < 64 || K > 4096) return TP_ERR_INVALID_ARG;
+    if ((which != 1 && which != 2) || (atom != 1 && atom != 2)) return TP_ERR_INVALID_ARG;
+    tp_gemm_opts o{};
+    o.atom = atom;
+    o.tile_n = 128;
+    o.no_tail = 1;
+    t_selftest_skip_commit = which;
+    t_selftest_limit_ns = static_cast<uint64_t>(limit_ms) * 1000000ull;
+    const int st = gemm_impl(A, B, C, M, N, K, K, K, N, 1, &o, 0, 0, nullptr, 0, stream);
+    t_selftest_skip_commit = 0;
     t_selftest_limit_ns = 0;
     return st;
 }

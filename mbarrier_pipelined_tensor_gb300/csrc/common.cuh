@@ -124,8 +124,53 @@ struct GemmParams {
     // producer withhold the expect_tx arrival of its first stage while still
     // issuing its loads, so the consumer's bounded wait must give up.
     int withhold_first_arrival;
+    // Self-test only (tp_selftest_mainloop_skipped_commit): 1 makes the MMA
+    // issuer skip its first commit to empty[s], 2 its first commit to
+    // acc_full[b], so the producer's or the epilogue's bounded wait must
+    // give up.
+    int skip_commit;
+    // Optional arrival accounting: kProtoSlots counters per CTA (below), or
+    // nullptr.
+    unsigned int* proto;
     WaitCtl wait;
 };
+
+// Arrival accounting (GemmParams::proto), per CTA, uint32 counters indexed
+// by barrier and phase: phase k of a barrier is the k-th time its stage (or
+// accumulator) is used. Arrivals are counted where they are issued, on the
+// CTA that owns the barrier (a 2-SM pair's full / acc_empty barriers are its
+// leader's; its commits arrive on both CTAs' empty / acc_full barriers).
+// Phases past the last counted one add to it.
+enum : int {
+    PROTO_MAX_STAGES = 9,
+    PROTO_PHASES = 64,
+    PROTO_BAR_FULL = 0,                                  // + stage
+    PROTO_BAR_EMPTY = PROTO_MAX_STAGES,                  // + stage
+    PROTO_BAR_ACC_FULL = 2 * PROTO_MAX_STAGES,           // + accumulator
+    PROTO_BAR_ACC_EMPTY = 2 * PROTO_MAX_STAGES + 2,      // + accumulator
+    PROTO_BARS = 2 * PROTO_MAX_STAGES + 4,
+    // transaction bytes of full[s] phase k: posted by expect_tx ...
+    PROTO_TX_EXPECT = PROTO_BARS * PROTO_PHASES,
+    // ... and carried by the TMA loads issued into it (both CTAs of a pair)
+    PROTO_TX_ISSUED = PROTO_TX_EXPECT + PROTO_MAX_STAGES * PROTO_PHASES,
+    kProtoSlots = PROTO_TX_ISSUED + PROTO_MAX_STAGES * PROTO_PHASES,
+};
+
+// Rows of PROTO_PHASES counters: barrier rows, then the two byte tables.
+enum : int {
+    PROTO_ROW_TX_EXPECT = PROTO_TX_EXPECT / PROTO_PHASES,
+    PROTO_ROW_TX_ISSUED = PROTO_TX_ISSUED / PROTO_PHASES,
+};
+
+// Adds v to phase `phase` of row `row` + `index` of CTA `cta`'s counters
+// (row: a PROTO_BAR_* barrier row or a PROTO_ROW_TX_* table; index: the
+// stage or accumulator).
+__device__ __forceinline__ void proto_add(unsigned int* proto, int cta, int row, int index, int phase,
+                                          unsigned int v)
+{
+    const int k = phase < PROTO_PHASES ? phase : PROTO_PHASES - 1;
+    atomicAdd(proto + static_cast<size_t>(cta) * kProtoSlots + (row + index) * PROTO_PHASES + k, v);
+}
 
 // Role-timeline counters, per CTA (GemmParams::trace).
 enum : int {

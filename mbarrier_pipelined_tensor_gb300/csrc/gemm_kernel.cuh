@@ -73,6 +73,7 @@ struct MainloopCfg {
                   "TMEM allocation must be a power of two");
     static_assert(BN % EPI_COLS == 0, "epilogue chunking");
     static_assert(2 * STAGES + 5 <= (BAR_BYTES - 8) / 8, "barrier area");
+    static_assert(STAGES <= PROTO_MAX_STAGES, "arrival accounting layout");
 };
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt)
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(192, 1)
 
     if (LDG && warp == 0) {
         // ------------------------------------- plain-load producer ---
-        int s = 0;
+        int s = 0, it = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
@@ -338,7 +339,11 @@ __global__ void __launch_bounds__(192, 1)
                                                   nt * BN, kb, lane);
                 fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(s));
+                if (lane == 0) {
+                    mbar_arrive(full_bar(s));
+                    if (p.proto) proto_add(p.proto, static_cast<int>(blockIdx.x), PROTO_BAR_FULL, s, it / STAGES, 1);
+                }
+                ++it;
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -360,9 +365,12 @@ __global__ void __launch_bounds__(192, 1)
             // choice is made once, by instantiating the loop for it; the
             // leader's full barriers are addressed from one mapa; the conv's
             // (tap, channel block) coordinates step instead of dividing.
-            auto run = [&](auto hint_a_t, auto hint_b_t) {
+            // PR: the instrumented loop (arrival accounting), instantiated
+            // apart so that the plain loop carries none of it.
+            auto run = [&](auto hint_a_t, auto hint_b_t, auto pr_t) {
                 constexpr bool HA = decltype(hint_a_t)::value;
                 constexpr bool HB = decltype(hint_b_t)::value;
+                constexpr bool PR = decltype(pr_t)::value;
                 const uint64_t pol_a = HA ? make_l2_policy(p.l2_a) : 0;
                 const uint64_t pol_b = HB ? make_l2_policy(p.l2_b) : 0;
                 const uint32_t fb0 = CL ? mapa_shared(full_bar(0), 0) : full_bar(0);
@@ -405,6 +413,17 @@ __global__ void __launch_bounds__(192, 1)
                         }
                         const uint32_t fb = fb0 + 8u * static_cast<uint32_t>(s);
                         if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), hu ? Cfg::TX_HALF_BYTES : Cfg::TX_BYTES);
+                        if constexpr (PR) {
+                            // phase issued / STAGES of stage s, on the leader's barrier
+                            const int lead = static_cast<int>(blockIdx.x) - static_cast<int>(rank);
+                            const int k = issued / STAGES;
+                            if (leader && arrive) {
+                                proto_add(p.proto, lead, PROTO_BAR_FULL, s, k, 1);
+                                proto_add(p.proto, lead, PROTO_ROW_TX_EXPECT, s, k, hu ? Cfg::TX_HALF_BYTES : Cfg::TX_BYTES);
+                            }
+                            proto_add(p.proto, lead, PROTO_ROW_TX_ISSUED, s, k,
+                                      Cfg::A_BYTES + (hu ? Cfg::B_BYTES / 2 : Cfg::B_BYTES));
+                        }
                         arrive = true;
                         const uint32_t dA = sA + s * Cfg::A_BYTES;
                         const uint32_t dB = sB + s * Cfg::B_BYTES;
@@ -460,13 +479,17 @@ __global__ void __launch_bounds__(192, 1)
             // priority asks for one (l2_a / l2_b != 0; 3 = explicit normal).
             using T = std::true_type;
             using F = std::false_type;
-            if (p.l2_a != 0) {
-                if (p.l2_b != 0) run(T{}, T{});
-                else run(T{}, F{});
-            } else {
-                if (p.l2_b != 0) run(F{}, T{});
-                else run(F{}, F{});
-            }
+            auto go = [&](auto pr) {
+                if (p.l2_a != 0) {
+                    if (p.l2_b != 0) run(T{}, T{}, pr);
+                    else run(T{}, F{}, pr);
+                } else {
+                    if (p.l2_b != 0) run(F{}, T{}, pr);
+                    else run(F{}, F{}, pr);
+                }
+            };
+            if (p.proto) go(T{});
+            else go(F{});
             if (p.trace) {
                 trace_add(p, TRACE_PRODUCER_SPAN, globaltimer_ns() - t_start);
                 trace_add(p, TRACE_PRODUCER_WAIT_EMPTY, t_wait);
@@ -508,42 +531,71 @@ __global__ void __launch_bounds__(192, 1)
                 // never carries): they are formed once and advanced by adds.
                 const uint64_t dA0 = umma_desc_sw128_kmajor(sA);
                 const uint64_t dB0 = umma_desc_sw128_kmajor(sB);
-                for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++lt) {
-                    const Unit w = unit_of(u, num_tiles, p);
-                    const int b = lt & 1;
-                    const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-                    if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
-                    if (p.events) event_at(p, lt, EV_MMA_START, globaltimer_ns());
-                    tcgen05_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-                    const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
-                    uint32_t accumulate = 0;  // the unit's first MMA overwrites the accumulator
-                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!timed_wait<CL>(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
-                            ok = false;
-                            break;
-                        }
+                // PR: the instrumented loop (arrival accounting and the
+                // skipped-commit self test), instantiated apart.
+                auto mma_run = [&](auto pr_t) {
+                    constexpr bool PR = decltype(pr_t)::value;
+                    int it = 0;  // stage uses so far (phase of stage s = it / STAGES)
+                    // Arrival of a commit on empty / acc_full barrier `bar` + `idx`,
+                    // phase k, in this CTA and (pair) its peer.
+                    [[maybe_unused]] auto count_commit = [&](int bar, int idx, int k) {
+                        proto_add(p.proto, static_cast<int>(blockIdx.x), bar, idx, k, 1);
+                        if constexpr (CL) proto_add(p.proto, static_cast<int>(blockIdx.x) + 1, bar, idx, k, 1);
+                    };
+                    for (int u = cluster_id; ok && u < num_units; u += num_clusters, ++lt) {
+                        const Unit w = unit_of(u, num_tiles, p);
+                        const int b = lt & 1;
+                        const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
+                        if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
+                        if (p.events) event_at(p, lt, EV_MMA_START, globaltimer_ns());
                         tcgen05_fence_after();
-                        const uint64_t da = dA0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
-                        const uint64_t db = dB0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
+                        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                        const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
+                        uint32_t accumulate = 0;  // the unit's first MMA overwrites the accumulator
+                        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                            if (!timed_wait<CL>(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
+                                ok = false;
+                                break;
+                            }
+                            tcgen05_fence_after();
+                            const uint64_t da = dA0 + static_cast<uint64_t>(s * (Cfg::A_BYTES >> 4));
+                            const uint64_t db = dB0 + static_cast<uint64_t>(s * (Cfg::B_BYTES >> 4));
 #pragma unroll
-                        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
-                            // +32 bytes per K step of 16 inside the swizzle atom
-                            umma_bf16<CG>(d_tmem, da + 2 * k, db + 2 * k, idesc, accumulate);
-                            accumulate = 1;
+                            for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
+                                // +32 bytes per K step of 16 inside the swizzle atom
+                                umma_bf16<CG>(d_tmem, da + 2 * k, db + 2 * k, idesc, accumulate);
+                                accumulate = 1;
+                            }
+                            bool commit = true;
+                            if constexpr (PR) {
+                                commit = !(p.skip_commit == 1 && it == 0);
+                                if (commit && p.proto) count_commit(PROTO_BAR_EMPTY, s, it / STAGES);
+                            }
+                            if (commit) {
+                                if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
+                                else umma_commit(empty_bar(s));
+                            }
+                            ++it;
+                            if (++s == STAGES) {
+                                s = 0;
+                                ph ^= 1u;
+                            }
                         }
-                        if constexpr (CL) umma_commit_pair(empty_bar(s), 0x3);
-                        else umma_commit(empty_bar(s));
-                        if (++s == STAGES) {
-                            s = 0;
-                            ph ^= 1u;
+                        if (!ok) break;
+                        if (p.events) event_at(p, lt, EV_MMA_END, globaltimer_ns());
+                        bool commit = true;
+                        if constexpr (PR) {
+                            commit = !(p.skip_commit == 2 && lt == 0);
+                            if (commit && p.proto) count_commit(PROTO_BAR_ACC_FULL, b, lt >> 1);
+                        }
+                        if (commit) {
+                            if constexpr (CL) umma_commit_pair(accf_bar(b), 0x3);
+                            else umma_commit(accf_bar(b));
                         }
                     }
-                    if (!ok) break;
-                    if (p.events) event_at(p, lt, EV_MMA_END, globaltimer_ns());
-                    if constexpr (CL) umma_commit_pair(accf_bar(b), 0x3);
-                    else umma_commit(accf_bar(b));
-                }
+                };
+                if (p.proto || p.skip_commit) mma_run(std::true_type{});
+                else mma_run(std::false_type{});
                 if (p.trace) {
                     trace_add(p, TRACE_MMA_SPAN, globaltimer_ns() - t_start);
                     trace_add(p, TRACE_MMA_WAIT_FULL, t_full);
@@ -594,6 +646,9 @@ __global__ void __launch_bounds__(192, 1)
                 if (lane == 0) {
                     if constexpr (CL) mbar_arrive_cluster(acce_target);
                     else mbar_arrive(acce_target);
+                    if (p.proto)
+                        proto_add(p.proto, static_cast<int>(blockIdx.x) - static_cast<int>(rank), PROTO_BAR_ACC_EMPTY,
+                                  b, lt >> 1, 1);
                 }
                 continue;
             }
@@ -626,6 +681,9 @@ __global__ void __launch_bounds__(192, 1)
                         if (p.events && warp == 2) event_at(p, lt, EV_EPI_RELEASED, globaltimer_ns());
                         if constexpr (CL) mbar_arrive_cluster(acce_target);
                         else mbar_arrive(acce_target);
+                        if (p.proto)
+                            proto_add(p.proto, static_cast<int>(blockIdx.x) - static_cast<int>(rank),
+                                      PROTO_BAR_ACC_EMPTY, b, lt >> 1, 1);
                     }
                 }
                 const int cs = n0 + c * Cfg::EPI_COLS;

@@ -58,7 +58,9 @@ class Deadlock(Exception):
     pass
 
 
-def simulate(CG, STAGES, tiles, KB, seed, bug=None, epi_warps=4):
+def simulate(CG, STAGES, tiles, KB, seed, bug=None, epi_warps=4, out=None):
+    """Runs the protocol; `out` (a dict), if given, receives the barriers
+    (keys full, empty, accf, acce: per CTA rank, per stage / accumulator)."""
     rng = random.Random(seed)
     full = [[MBarrier(f"full{r}[{s}]", 1) for s in range(STAGES)] for r in range(CG)]
     empty = [[MBarrier(f"empty{r}[{s}]", 1) for s in range(STAGES)] for r in range(CG)]
@@ -174,6 +176,8 @@ def simulate(CG, STAGES, tiles, KB, seed, bug=None, epi_warps=4):
     for t in tiles:
         for r in range(CG):
             assert sorted(outputs[(t, r)]) == list(range(epi_warps))
+    if out is not None:
+        out.update(full=full, empty=empty, accf=accf, acce=acce)
     return steps
 
 
