@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(32, 1)
         for (; i < n_my; ++i) {
             const int s = i % STAGES;
             const uint32_t ph = static_cast<uint32_t>(i / STAGES) & 1u;
-            if (!wait_bounded<false>(full_bar(s), ph, p.wait, abort_flag, SITE_COPY_FULL)) break;
+            if (!wait_bounded(full_bar(s), ph, p.wait, abort_flag, SITE_COPY_FULL)) break;
             int x, y;
             tile_xy(i, x, y);
             tma_store_2d(&dst, base + s * stride, x, y);
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(32, 1)
             // Gave up: let every load still in flight land (bounded) before exit.
             volatile int no_abort = 0;
             for (int k = i; k < loaded; ++k)
-                wait_bounded<false>(full_bar(k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u, p.wait,
+                wait_bounded(full_bar(k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u, p.wait,
                                     &no_abort, SITE_DRAIN);
         }
         // Epilogue: drain every outstanding store.
@@ -208,7 +208,7 @@ __global__ void wait_timeout_selftest_kernel(WaitCtl w)
         mbar_init(smem_u32(&bar), 1);
         abort_flag = 0;
         fence_mbarrier_init();
-        wait_bounded<false>(smem_u32(&bar), 0, w, reinterpret_cast<volatile int*>(&abort_flag), SITE_SELFTEST);
+        wait_bounded(smem_u32(&bar), 0, w, reinterpret_cast<volatile int*>(&abort_flag), SITE_SELFTEST);
     }
 }
 

@@ -233,13 +233,12 @@ __device__ __forceinline__ void event_at(const GemmParams& p, int lt, int ev, un
 }
 
 // Bounded wait that charges its duration to a timeline slot.
-template <bool CL>
 __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int site, unsigned long long& acc)
 {
-    if (!p.trace) return wait_bounded<CL>(bar, parity, p.wait, abort_flag, site);
+    if (!p.trace) return wait_bounded(bar, parity, p.wait, abort_flag, site);
     const uint64_t t0 = globaltimer_ns();
-    const bool ok = wait_bounded<CL>(bar, parity, p.wait, abort_flag, site);
+    const bool ok = wait_bounded(bar, parity, p.wait, abort_flag, site);
     acc += globaltimer_ns() - t0;
     return ok;
 }
@@ -330,7 +329,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 int free_ok = 1;
                 if (lane == 0)
-                    free_ok = wait_bounded<false>(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
+                    free_ok = wait_bounded(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
                 if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
                     ok = false;
                     break;
@@ -407,7 +406,7 @@ __global__ void __launch_bounds__(192, 1)
                         sx = rs - r * p.conv_S;
                     }
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                        if (!timed_wait<CL>(p, empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY, t_wait)) {
+                        if (!timed_wait(p, empty_bar(s), ph ^ 1u, abort_flag, SITE_PRODUCER_EMPTY, t_wait)) {
                             ok = false;
                             break;
                         }
@@ -507,7 +506,7 @@ __global__ void __launch_bounds__(192, 1)
                         ss = STAGES - 1;
                         pp ^= 1u;
                     }
-                    wait_bounded<CL>(full_bar(ss), pp, drain, &no_abort, SITE_DRAIN);
+                    wait_bounded(full_bar(ss), pp, drain, &no_abort, SITE_DRAIN);
                 }
             }
         }
@@ -546,14 +545,14 @@ __global__ void __launch_bounds__(192, 1)
                         const Unit w = unit_of(u, num_tiles, p);
                         const int b = lt & 1;
                         const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-                        if (!timed_wait<CL>(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
+                        if (!timed_wait(p, acce_bar(b), aph ^ 1u, abort_flag, SITE_MMA_ACC_EMPTY, t_acc)) break;
                         if (p.events) event_at(p, lt, EV_MMA_START, globaltimer_ns());
                         tcgen05_fence_after();
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
                         const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
                         uint32_t accumulate = 0;  // the unit's first MMA overwrites the accumulator
                         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                            if (!timed_wait<CL>(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
+                            if (!timed_wait(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
                                 ok = false;
                                 break;
                             }
@@ -606,7 +605,7 @@ __global__ void __launch_bounds__(192, 1)
                 if constexpr (CL) umma_commit_pair(drain_bar, 0x1);
                 else umma_commit(drain_bar);
                 volatile int no_abort = 0;
-                wait_bounded<CL>(drain_bar, 0, p.wait, &no_abort, SITE_DRAIN);
+                wait_bounded(drain_bar, 0, p.wait, &no_abort, SITE_DRAIN);
             }
             __syncwarp();
         }
@@ -624,7 +623,7 @@ __global__ void __launch_bounds__(192, 1)
             const Unit w = unit_of(u, num_tiles, p);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-            if (!timed_wait<CL>(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
+            if (!timed_wait(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
             if (p.events && warp == 2 && lane == 0) event_at(p, lt, EV_EPI_READY, globaltimer_ns());
             tcgen05_fence_after();
             int mt, nt;

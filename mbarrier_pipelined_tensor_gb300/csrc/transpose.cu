@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(32)
         const int s = i % STAGES;
         int ok = 1;
         if (leader)
-            ok = wait_bounded<false>(full_bar(s), static_cast<uint32_t>(i / STAGES) & 1u, p.wait, abort_flag,
+            ok = wait_bounded(full_bar(s), static_cast<uint32_t>(i / STAGES) & 1u, p.wait, abort_flag,
                                      SITE_COPY_FULL);
         // The leader lane's result decides for the warp (elect_one's lane).
         ok = __any_sync(0xffffffffu, leader && ok) ? 1 : 0;
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(32)
             volatile int no_abort = 0;
             const int last = (i + STAGES < n_my ? i + STAGES : n_my);
             for (int k = i; k < last; ++k)
-                wait_bounded<false>(full_bar(k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u, p.wait,
+                wait_bounded(full_bar(k % STAGES), static_cast<uint32_t>(k / STAGES) & 1u, p.wait,
                                     &no_abort, SITE_DRAIN);
         }
         bulk_wait_group<0>();
