@@ -355,6 +355,23 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
     rows["conv_32x56x56x256_3x3"] = {"unit": "TFLOP/s", "l2": "flushed between calls", **conv_res}
     del xd, wd, y
 
+    # TMA read stream of a 256 MiB operand (the skinny GEMM's B, 8192 x 16384):
+    # the measured bound of a GEMM that streams B once, with the same write
+    # flush before each timed call as the GEMM rows.
+    rr, cc = 8192, 16384
+    rbuf = torch.zeros((rr, cc), dtype=torch.int16, device="cuda")
+    rd = lambda: tp.tp_tma_read_2d(rbuf, rr, cc, cc, stream=s)  # noqa: E731
+    for _ in range(3):
+        rd()
+    med_r, _ = time_each_flushed(torch, stream, rd, 20, flush_buf)
+    b2b_r = time_loop(torch, stream, rd, 20) / 20
+    read_gbs = rr * cc * 2 / (med_r * 1e-3) / 1e9
+    rows["tma_read_stream_256MiB"] = {"unit": "GB/s", "flushed_gbs": round(read_gbs, 1), "us_flushed": round(med_r * 1e3, 2),
+                                      "b2b_gbs": round(rr * cc * 2 / (b2b_r * 1e-3) / 1e9, 1),
+                                      "frac_of_hbm_copy": round(read_gbs / peaks["hbm_gbs"], 3),
+                                      "plan": {k: tp.tp_last_plan()[k] for k in ("pipe_depth", "grid")}}
+    del rbuf
+
     # skinny set (uniform seed 3)
     sk = {}
     for (Ms, Ns, Ks), (A, B) in zip(datagen.SKINNY_SHAPES, datagen.skinny_operands()):
@@ -372,8 +389,11 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         byts = 2.0 * (Ms * Ks + Ns * Ks + Ms * Ns)
         tfl = f / (med * 1e-3) / 1e12
         bound = min(peaks["bf16_tflops"], f / byts * peaks["hbm_gbs"] * 1e9 / 1e12)
+        # the same bound with the measured read stream in place of the copy peak
+        read_bound = min(peaks["bf16_tflops"], f / byts * read_gbs * 1e9 / 1e12)
         row = {"us": round(med * 1e3, 2), "tflops": round(tfl, 1), "roofline_tflops": round(bound, 1),
-               "frac": round(tfl / bound, 3), "grid": tp.tp_last_plan()["grid"]}
+               "frac": round(tfl / bound, 3), "read_bound_tflops": round(read_bound, 1),
+               "read_frac": round(tfl / read_bound, 3), "grid": tp.tp_last_plan()["grid"]}
         row["role_timeline"] = role_timeline(
             torch, tp, lambda tr: tp.tp_gemm_bf16_ex(a, b, c, Ms, Ns, Ks, Ks, Ks, Ns, stream=s, trace=tr))
         # split-K with a caller workspace (slices chosen by the library)
@@ -388,6 +408,7 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         pl = tp.tp_last_plan()
         tfl_s = f / (med_s * 1e-3) / 1e12
         row["splitk"] = {"us": round(med_s * 1e3, 2), "tflops": round(tfl_s, 1), "frac": round(tfl_s / bound, 3),
+                         "read_frac": round(tfl_s / read_bound, 3),
                          "splits": pl["splits"], "grid": pl["grid"], "atom": pl["atom"], "tile_n": pl["tile_n"]}
         sk[f"{Ms}x{Ns}x{Ks}"] = row
         del a, b, c, ws
@@ -658,10 +679,15 @@ def summarize(value, achieved, peak, rows, sweep, peaks):
                 continue
             e = {"tflops": r["tflops"], "us": r["us"], "frac": r["frac"], "bound_tflops": r["roofline_tflops"],
                  "cublas_tflops": lib.get(f"gemm_{key}", {}).get("tflops")}
+            if r.get("read_bound_tflops", 0) < r["roofline_tflops"] and "read_frac" in r:
+                e["read_bound_tflops"] = r["read_bound_tflops"]
+                e["read_frac"] = r["read_frac"]
             sk = r.get("splitk")
             if sk and sk.get("splits", 1) > 1:
                 e["splitk_tflops"] = sk["tflops"]
                 e["splitk_frac"] = sk["frac"]
+                if "read_frac" in e and "read_frac" in sk:
+                    e["splitk_read_frac"] = sk["read_frac"]
                 e["splits"] = sk["splits"]
             out[f"gemm_{key}"] = e
         sm = rows.get("gemm_320x200x448_f32")
@@ -673,6 +699,9 @@ def summarize(value, achieved, peak, rows, sweep, peaks):
             if r:
                 out[key] = {"gbs": r["gbs"], "frac": r["frac_of_hbm"], "bit_exact": r["bit_exact"],
                             "torch_gbs": lib.get(lk, {}).get("gbs")}
+        rs = rows.get("tma_read_stream_256MiB")
+        if rs:
+            out["tma_read_stream_256MiB"] = {"flushed_gbs": rs["flushed_gbs"], "b2b_gbs": rs["b2b_gbs"]}
         fb = rows.get("fallback_paths", {})
         if "plain_load_producer_4096" in fb:
             out["plain_load_producer_4096"] = {"tflops": fb["plain_load_producer_4096"]["tflops"],

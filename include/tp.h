@@ -65,7 +65,8 @@ enum {
     TP_PATH_VEC_COPY = 4,      /* vectorized ld/st fallback copy */
     TP_PATH_FALLBACK_MAINLOOP = 5, /* plain-load producer + tcgen05 mainloop */
     TP_PATH_TMA_TRANSPOSE = 6,     /* TMA load -> ldmatrix/stmatrix.trans -> TMA store */
-    TP_PATH_VEC_TRANSPOSE = 7      /* shared-memory tile transpose fallback */
+    TP_PATH_VEC_TRANSPOSE = 7,     /* shared-memory tile transpose fallback */
+    TP_PATH_TMA_READ = 8           /* TMA load ring only (tp_tma_read_2d) */
 };
 
 /*
@@ -367,6 +368,21 @@ TP_API int tp_tma_transpose_2d(const void* src, void* dst, int64_t rows, int64_t
  * tile is 64x64). */
 TP_API int tp_tma_transpose_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src,
                                   int64_t ld_dst, const tp_copy_opts* opts, void* stream);
+
+/*
+ * Streams a rows x cols matrix of 2-byte elements (row pitch `ld` elements)
+ * through the TMA load ring of the copy -- persistent one-warp CTAs, each
+ * taking a contiguous run of box_rows x box_cols tiles through a
+ * stages-deep ring -- and discards it: the load half of "B200 Tma Pipeline
+ * Designer" steps 4-7 on its own, with no store traffic beside it. It
+ * measures how fast the GPU pulls an operand (the bound of a skinny GEMM
+ * that streams its B once). opts may be NULL (128 x 64 tiles, 8 stages, one
+ * CTA per SM); stages in {2, 4, 8, 12}. src must be 16-byte aligned with a
+ * pitch of whole 16-byte granules and cols a multiple of 8
+ * (TP_ERR_UNSUPPORTED otherwise: there is no fallback). Reads only.
+ */
+TP_API int tp_tma_read_2d(const void* src, int64_t rows, int64_t cols, int64_t ld, const tp_copy_opts* opts,
+                          void* stream);
 
 /* Synchronizes `stream`, returns the current device's status (TP_OK or the
  * first device-side failure since the last call, e.g. TP_ERR_TIMEOUT from a

@@ -41,6 +41,7 @@ TP_PATH_VEC_COPY = 4
 TP_PATH_FALLBACK_MAINLOOP = 5
 TP_PATH_TMA_TRANSPOSE = 6
 TP_PATH_VEC_TRANSPOSE = 7
+TP_PATH_TMA_READ = 8
 
 
 class tp_gemm_opts(ctypes.Structure):
@@ -92,6 +93,7 @@ _SIGS = {
     "tp_tma_copy_2d_ex": ([_P, _P, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
     "tp_tma_transpose_2d": ([_P, _P, _I64, _I64, _I64, _I64, _P], _I),
     "tp_tma_transpose_2d_ex": ([_P, _P, _I64, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
+    "tp_tma_read_2d": ([_P, _I64, _I64, _I64, ctypes.POINTER(tp_copy_opts), _P], _I),
     "tp_device_status": ([_P], _I),
     "tp_device_status_detail": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "tp_status_string": ([_I], ctypes.c_char_p),
@@ -293,6 +295,13 @@ def tp_tma_transpose_2d_ex(src, dst, rows, cols, ld_src, ld_dst, stream=None, st
     o = tp_copy_opts(0, 0, stages, ctas_per_sm, int(bool(force_vec)))
     _check(_lib.tp_tma_transpose_2d_ex(_ptr(src), _ptr(dst), rows, cols, ld_src, ld_dst, ctypes.byref(o),
                                        _stream(stream)), "tp_tma_transpose_2d_ex")
+
+
+def tp_tma_read_2d(src, rows, cols, ld, stream=None, box_cols=0, box_rows=0, stages=0, ctas_per_sm=0):
+    """Streams rows x cols 2-byte elements (pitch `ld`) through the TMA load ring and discards
+    them: how fast the GPU pulls an operand. Options 0 = library default."""
+    o = tp_copy_opts(box_cols, box_rows, stages, ctas_per_sm, 0)
+    _check(_lib.tp_tma_read_2d(_ptr(src), rows, cols, ld, ctypes.byref(o), _stream(stream)), "tp_tma_read_2d")
 
 
 def tp_device_status(stream=None) -> int:

@@ -33,6 +33,7 @@ cudaError_t launch_splitk_reduce(const float* ws, void* C, int M, int N, int64_t
 cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensorMap& d, const CopyParams& p,
                                 int grid, cudaStream_t st);
 int copy_smem_bytes(int stages, uint32_t tile_bytes);
+cudaError_t launch_tma_read_any(int stages, const CUtensorMap& s, const CopyParams& p, int grid, cudaStream_t st);
 cudaError_t launch_vec_copy(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld, int sm_count,
                             cudaStream_t st);
 cudaError_t launch_zero_fill(void* c, int64_t M, int64_t N, int64_t ldc, int elem_bytes, cudaStream_t st);
@@ -913,6 +914,62 @@ int tp_tma_copy_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, in
 int tp_tma_copy_2d(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld, void* stream)
 {
     return tp_tma_copy_2d_ex(src, dst, rows, cols, ld, nullptr, stream);
+}
+
+int tp_tma_read_2d(const void* src, int64_t rows, int64_t cols, int64_t ld, const tp_copy_opts* o, void* stream)
+{
+    tp_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    t_last_plan = pl;
+    if (rows < 0 || cols < 0 || ld < cols) return TP_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return TP_OK;
+    if (!src) return TP_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st) return st;
+    // Defaults from a sweep on GB300 (256 MiB after a 256 MiB write flush):
+    // 128 x 64 tiles, 8 stages, one CTA per SM, 57 us (4.7 TB/s); 42.5 us
+    // back to back.
+    const int box_cols = o && o->box_cols ? o->box_cols : 64;
+    const int box_rows = o && o->box_rows ? o->box_rows : 128;
+    const int stages = o && o->stages ? o->stages : 8;
+    const int per_sm = o && o->ctas_per_sm ? o->ctas_per_sm : 1;
+    if (box_cols < 8 || box_cols > 256 || (box_cols * 2) % 16 || box_rows < 1 || box_rows > 256 || per_sm < 1 ||
+        (stages != 2 && stages != 4 && stages != 8 && stages != 12))
+        return TP_ERR_INVALID_ARG;
+    // TMA only: rows of whole 16-byte granules at a 16-byte aligned base.
+    if (!aligned16(src) || (ld * 2) % 16 || cols % 8 || rows > INT32_MAX || cols > INT32_MAX)
+        return TP_ERR_UNSUPPORTED;
+    const uint32_t tile_bytes = static_cast<uint32_t>(box_cols * box_rows * 2);
+    const int smem = copy_smem_bytes(stages, tile_bytes);
+    if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
+    TiledDesc d{CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(src),
+                {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)}, {static_cast<uint64_t>(ld) * 2},
+                {static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows)}, CU_TENSOR_MAP_SWIZZLE_NONE};
+    CUtensorMap ms;
+    if ((st = encode_tiled(&ms, d))) return st;
+    CopyParams p{};
+    p.tiles_x = static_cast<int>(cdiv(cols, box_cols));
+    p.tiles_y = static_cast<int>(cdiv(rows, box_rows));
+    p.box_cols = box_cols;
+    p.box_rows = box_rows;
+    p.tile_bytes = tile_bytes;
+    p.wait = WaitCtl{dev->status, wait_limit_ns()};
+    const int64_t tiles = static_cast<int64_t>(p.tiles_x) * p.tiles_y;
+    if (tiles > INT32_MAX) return TP_ERR_UNSUPPORTED;
+    int64_t grid = static_cast<int64_t>(dev->sm_count) * per_sm;
+    if (grid > tiles) grid = tiles;
+    cudaError_t e = launch_tma_read_any(stages, ms, p, static_cast<int>(grid), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    pl.path = TP_PATH_TMA_READ;
+    pl.pipe_depth = stages;
+    pl.grid = static_cast<int>(grid);
+    pl.cluster = 1;
+    pl.smem_bytes = smem;
+    pl.m_tiles = p.tiles_y;
+    pl.n_tiles = p.tiles_x;
+    t_last_plan = pl;
+    return TP_OK;
 }
 
 int tp_tma_transpose_2d_ex(const void* src, void* dst, int64_t rows, int64_t cols, int64_t ld_src, int64_t ld_dst,

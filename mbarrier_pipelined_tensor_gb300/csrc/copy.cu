@@ -126,6 +126,96 @@ cudaError_t launch_tma_copy_any(int stages, const CUtensorMap& s, const CUtensor
     }
 }
 
+// ---------------------------------------------------------- read stream ---
+//
+// The load half of the copy ring on its own: each CTA streams a contiguous
+// run of tiles through its STAGES-deep ring and discards them. It measures
+// how fast TMA can pull an operand out of memory -- the bound of a GEMM that
+// only streams its B (a skinny M) -- with no store traffic beside it. The
+// loop steps tile coordinates incrementally: one thread issues every load.
+template <int STAGES>
+__global__ void __launch_bounds__(32, 1)
+    tma_read_kernel(const __grid_constant__ CUtensorMap src, const CopyParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t stride = (p.tile_bytes + 1023u) & ~1023u;
+    const uint32_t sBar = base + STAGES * stride;
+    volatile int* const abort_flag =
+        reinterpret_cast<volatile int*>(smem_raw + (sBar - raw) + 8 * STAGES);
+    auto full_bar = [&](int s) { return sBar + 8u * s; };
+
+    if (elect_one()) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(full_bar(s), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tensormap(&src);
+        const int total = p.tiles_x * p.tiles_y;
+        const int chunk = (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+        const int first = static_cast<int>(blockIdx.x) * chunk;
+        const int count = min(chunk, total - first);
+        int tx = first % p.tiles_x, ty = first / p.tiles_x;
+        int s = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int c = 0; c < count; ++c) {
+            // stage s was last filled STAGES tiles ago, in the ring pass of parity ph ^ 1
+            if (issued >= STAGES && !wait_bounded(full_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_COPY_FULL)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(full_bar(s), p.tile_bytes);
+            tma_load_2d(base + s * stride, &src, full_bar(s), tx * p.box_cols, ty * p.box_rows);
+            ++issued;
+            if (++s == STAGES) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++tx == p.tiles_x) {
+                tx = 0;
+                ++ty;
+            }
+        }
+        // Every load still in flight lands before the CTA exits (bounded).
+        volatile int no_abort = 0;
+        const int n = issued < STAGES ? issued : STAGES;
+        for (int k = 0; k < n; ++k) {
+            if (--s < 0) {
+                s = STAGES - 1;
+                ph ^= 1u;
+            }
+            wait_bounded(full_bar(s), ph, p.wait, ok ? abort_flag : &no_abort, SITE_DRAIN);
+        }
+    }
+    __syncwarp();
+}
+
+template <int STAGES>
+cudaError_t launch_tma_read(const CUtensorMap& s, const CopyParams& p, int grid, cudaStream_t st)
+{
+    const uint32_t stride = (p.tile_bytes + 1023u) & ~1023u;
+    const int smem = 1024 + STAGES * static_cast<int>(stride) + 8 * STAGES + 16;
+    auto kern = tma_read_kernel<STAGES>;
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = smem_limit_once(kern, 232448, smem_set);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 32, smem, st>>>(s, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tma_read_any(int stages, const CUtensorMap& s, const CopyParams& p, int grid, cudaStream_t st)
+{
+    switch (stages) {
+    case 2: return launch_tma_read<2>(s, p, grid, st);
+    case 4: return launch_tma_read<4>(s, p, grid, st);
+    case 8: return launch_tma_read<8>(s, p, grid, st);
+    case 12: return launch_tma_read<12>(s, p, grid, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // ------------------------------------------------------------ fallback ---
 
 // rows x row_elems 2-byte elements, both buffers with pitch `pitch` elements.
