@@ -155,13 +155,15 @@ const KernelEntry* find_kernel(const KernelKey& k)
     return nullptr;
 }
 
-// Mirrors MainloopCfg::SMEM_BYTES.
-int64_t mainloop_smem(int atom, int depth, int tile_n)
+// Mirrors MainloopCfg::SMEM_BYTES (plus, for the plain-load producer, its
+// staging buffers).
+int64_t mainloop_smem(int atom, int depth, int tile_n, int ldg = 0)
 {
     const int64_t a = 128 * 64 * 2;
     const int64_t b = static_cast<int64_t>(tile_n / atom) * 64 * 2;
     const int64_t epi = 4 * 2 * 32 * 128;
-    return 1024 + depth * (a + b) + epi + 256;
+    const int64_t staging = ldg ? static_cast<int64_t>(kLdgStaging) * (128 + tile_n / atom) * kLdgWindow : 0;
+    return 1024 + depth * (a + b) + epi + 256 + staging;
 }
 
 int deepest_fitting(int atom, int tile_n)
@@ -249,9 +251,11 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     if ((atom == 0 || tile_n == 0) &&
         !choose_variant(M, N, k_blocks, sm_count, out_f32, conv, splitk, &atom, &tile_n))
         return TP_ERR_UNSUPPORTED;
-    int depth = o && o->pipe_depth ? o->pipe_depth : deepest_fitting(atom, tile_n);
+    // The plain-load producer stages its copies outside the ring, which
+    // leaves room for kLdgStages ring stages.
+    int depth = o && o->pipe_depth ? o->pipe_depth : (ldg ? kLdgStages : deepest_fitting(atom, tile_n));
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
-    const int64_t smem = mainloop_smem(atom, depth, tile_n);
+    const int64_t smem = mainloop_smem(atom, depth, tile_n, ldg);
     if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
     const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv, ldg, 0});
     if (!k) return TP_ERR_UNSUPPORTED;

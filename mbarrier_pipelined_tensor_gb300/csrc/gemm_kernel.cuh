@@ -23,11 +23,16 @@
 //
 // Plain-load producer (LDG = true, 1-SM only): for operands TMA cannot
 // describe ("B200 Tma Pipeline Designer", step 1: keep the vectorized thread
-// copy), all 32 lanes of warp 0 gather the stage with global loads, bounds
-// checked element by element, and write it in the same 128-byte-swizzled
-// layout TMA would produce; each lane fences its generic-proxy writes for the
-// tensor core's async-proxy reads, and one lane makes the stage's single
-// arrival. The epilogue then writes C with plain stores.
+// copy), four producer warps (0 and 6-8) each own a quarter of a stage's
+// rows. A row's 64-element K segment starts at an address that is only
+// 2-byte aligned, so the warp copies the 144-byte window of 16-byte aligned
+// chunks around it with cp.async into a staging buffer (no registers hold
+// loads in flight; the copies of the next stage are issued before the
+// current one is unpacked), then shifts each row into place and writes it
+// in the same 128-byte-swizzled layout TMA would produce. Each warp fences
+// its generic-proxy writes for the tensor core's async-proxy reads and
+// makes one arrival on the stage's full barrier. The epilogue then writes C
+// with plain stores.
 //
 // Atoms ("two-free-pipeline-stages" note): CG = 1 is the 1-SM atom (each CTA
 // owns a 128 x BN tile and holds all of its B tile); CG = 2 is the 2-SM atom
@@ -102,94 +107,189 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// 8 consecutive bf16 (one 16-byte chunk of a swizzle row) gathered with
-// bounds checks; out-of-range elements are zero, as TMA's fill would be.
-// row_ptr must point at a readable row even when row_ok is false. Every load
-// is issued unconditionally, from element 0 of that row when its own element
-// is out of range, so the loads of several chunks can be in flight at once.
-__device__ __forceinline__ void gather8(const uint16_t* __restrict__ row_ptr, bool row_ok, int col0, int cols,
-                                        uint32_t (&v)[4])
+// The plain-load producer: producer warps, staging buffers (each holds a
+// stage's rows as 144-byte windows of aligned 16-byte chunks, then one
+// 32-bit code per row), and ring depth.
+constexpr int kLdgWarps = 8;
+constexpr int kLdgStaging = 2;
+constexpr int kLdgStages = 3;
+constexpr int kLdgWindow = 144;
+
+template <int B_ROWS>
+__host__ __device__ constexpr int ldg_staging_buffer_bytes()
 {
+    return (128 + B_ROWS) * (kLdgWindow + 4);
+}
+
+template <int B_ROWS>
+__host__ __device__ constexpr int ldg_staging_bytes()
+{
+    return kLdgStaging * ldg_staging_buffer_bytes<B_ROWS>();
+}
+
+// Row of the stage that lane `sub` (0..3) of a producer warp handles in row
+// quad q: the quad's four rows are 8 apart, so that in a GEMM operand
+// (whose row pitch repeats its 16-byte alignment every 8 rows) all four
+// shift by the same amount.
+__device__ __forceinline__ int ldg_row(int pw, int rpw, int q, int sub)
+{
+    return pw * rpw + (q & 7) + 8 * (4 * (q >> 3) + sub);
+}
+
+// Where stage row `row` (A: rows 0..127, B: 128..) of K block kb comes
+// from: the address of its first element (0 when the row is out of range)
+// and the number of valid elements from there (1..64). The operand fields
+// are copied out of the kernel parameters once.
+template <bool CONV>
+struct LdgRows {
+    const uint16_t* A;
+    const uint16_t* B;
+    int64_t lda, ldb;
+    int M, N, m_row, n_row, c0, r, sx, nvalid;
+    int P, Q, H, W, C, R, S, stride, pad;
+
+    __device__ __forceinline__ LdgRows(const GemmParams& p, int m0, int n0, int kb)
+        : A(p.A), B(p.B), lda(p.lda), ldb(p.ldb), M(p.M), N(p.N), m_row(m0), n_row(n0)
+    {
+        r = 0;
+        sx = 0;
+        c0 = kb * 64;
+        if constexpr (CONV) {
+            const int rs = kb / p.conv_cblocks;
+            c0 = (kb - rs * p.conv_cblocks) * 64;
+            r = rs / p.conv_S;
+            sx = rs - r * p.conv_S;
+            P = p.conv_P;
+            Q = p.conv_Q;
+            H = p.conv_H;
+            W = p.conv_W;
+            C = p.conv_C;
+            R = p.conv_R;
+            S = p.conv_S;
+            stride = p.conv_stride;
+            pad = p.conv_pad;
+        }
+        const int width = CONV ? p.conv_C : p.K;
+        nvalid = (width - c0) < 64 ? (width - c0) : 64;  // >= 1: c0 < width
+    }
+
+    __device__ __forceinline__ uintptr_t segment(int row) const
+    {
+        if (row < 128) {
+            const int m = m_row + row;
+            if constexpr (CONV) {
+                const int pq = P * Q;
+                const int img = m / pq;
+                const int rem = m - img * pq;
+                const int pp = rem / Q;
+                const int qq = rem - pp * Q;
+                const int h = pp * stride - pad + r;
+                const int w = qq * stride - pad + sx;
+                if (m >= M || h < 0 || h >= H || w < 0 || w >= W) return 0;
+                return reinterpret_cast<uintptr_t>(A + ((static_cast<int64_t>(img) * H + h) * W + w) * C + c0);
+            } else {
+                if (m >= M) return 0;
+                return reinterpret_cast<uintptr_t>(A + static_cast<int64_t>(m) * lda + c0);
+            }
+        }
+        const int n = n_row + (row - 128);
+        if (n >= N) return 0;
+        if constexpr (CONV)
+            return reinterpret_cast<uintptr_t>(B + ((static_cast<int64_t>(n) * R + r) * S + sx) * C + c0);
+        else
+            return reinterpret_cast<uintptr_t>(B + static_cast<int64_t>(n) * ldb + c0);
+    }
+};
+
+// Issues the cp.async copies of rows [pw * RPW, pw * RPW + RPW) of one stage
+// into staging buffer `stg`: lane j of a row's eight copies aligned chunk j
+// of the 144-byte window that starts at the row's address rounded down to 16
+// bytes (lane 7 also chunk 8), and lane 0 records the row's code: the
+// window's first valid byte (a & 15) and one past its last (0: row out of
+// range). A chunk is copied only if it holds at least one element of the
+// row's valid range, so no access touches a 16-byte block outside the
+// operand (and none crosses a page).
+template <int B_ROWS, bool CONV, int RPW>
+__device__ __forceinline__ void ldg_issue_rows(const LdgRows<CONV>& rows, uint32_t stg, int pw, uint32_t lane)
+{
+    const int sub = static_cast<int>(lane >> 3);
+    const uint32_t j = lane & 7u;
+    const uint32_t codes = stg + (128 + B_ROWS) * kLdgWindow;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int c = col0 + 2 * e;
-        const bool lo_ok = row_ok && c < cols;
-        const bool hi_ok = row_ok && c + 1 < cols;
-        const uint32_t lo = __ldg(row_ptr + (lo_ok ? c : 0));
-        const uint32_t hi = __ldg(row_ptr + (hi_ok ? c + 1 : 0));
-        v[e] = (lo_ok ? lo : 0u) | ((hi_ok ? hi : 0u) << 16);
+    for (int q = 0; q < RPW / 4; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        const uintptr_t a = rows.segment(row);
+        const uint32_t mis = static_cast<uint32_t>(a & 15u);
+        const uint32_t end = a ? mis + 2u * static_cast<uint32_t>(rows.nvalid) : 0u;
+        if (j == 0u) st_shared_u32(codes + 4u * static_cast<uint32_t>(row), mis | (end << 8));
+        const uintptr_t base = a - mis;
+        const uint32_t dst = stg + static_cast<uint32_t>(row) * kLdgWindow;
+        if (16u * j < end) cp_async_16(dst + 16u * j, base + 16u * j);
+        if (j == 7u && 128u < end) cp_async_16(dst + 128u, base + 128u);
     }
 }
 
-// Fills one stage (A: 128 rows, B: B_ROWS rows, 64 bf16 each) with plain
-// loads; lane L handles chunks L, L+32, ... (8 chunks per 128-byte row). The
-// loads of kBatch chunks per lane are issued before any of them is stored.
-template <int B_ROWS, bool CONV>
-__device__ __forceinline__ void ldg_fill_stage(const GemmParams& p, uint32_t dA, uint32_t dB, int m_row, int n_row,
-                                               int kb, uint32_t lane)
+// Shifts the staged rows [pw * RPW, pw * RPW + RPW) into place: output chunk
+// j of a row is bytes (a & 15) + 16 j .. + 15 of its window, picked with
+// word selects and a 16-bit funnel shift. Chunks that were not copied,
+// elements past the valid range and rows out of range read as zero, as
+// TMA's fill would.
+template <int B_ROWS, int RPW>
+__device__ __forceinline__ void ldg_repack_rows(uint32_t stg, int nvalid, uint32_t dA, uint32_t dB, int pw,
+                                                uint32_t lane)
 {
-    constexpr int kBatch = 8;
-    static_assert((128 * 8) % (32 * kBatch) == 0 && (B_ROWS * 8) % (32 * kBatch) == 0, "whole batches");
-    int r = 0, sx = 0, c0 = kb * 64;
-    if constexpr (CONV) {
-        const int rs = kb / p.conv_cblocks;
-        c0 = (kb - rs * p.conv_cblocks) * 64;
-        r = rs / p.conv_S;
-        sx = rs - r * p.conv_S;
+    const int sub = static_cast<int>(lane >> 3);
+    const uint32_t j = lane & 7u;
+    const uint32_t codes = stg + (128 + B_ROWS) * kLdgWindow;
+    const bool full_k = nvalid == 64;
+    constexpr int kQuads = RPW / 4;
+    // every quad's shared-memory reads first, so their latencies overlap
+    uint32_t mis[kQuads], end[kQuads];
+    uint4 lo[kQuads], hi[kQuads];
+#pragma unroll
+    for (int q = 0; q < kQuads; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        const uint32_t code = ld_shared_u32(codes + 4u * static_cast<uint32_t>(row));
+        mis[q] = code & 0xFFu;
+        end[q] = code >> 8;
     }
-    auto load_a = [&](int idx, uint32_t (&v)[4]) {
-        const int row = idx >> 3, j = idx & 7;
-        const int m = m_row + row;
-        if constexpr (CONV) {
-            const int pq = p.conv_P * p.conv_Q;
-            const int img = m / pq;
-            const int rem = m - img * pq;
-            const int pp = rem / p.conv_Q;
-            const int qq = rem - pp * p.conv_Q;
-            const int h = pp * p.conv_stride - p.conv_pad + r;
-            const int w = qq * p.conv_stride - p.conv_pad + sx;
-            const bool ok = m < p.M && h >= 0 && h < p.conv_H && w >= 0 && w < p.conv_W;
-            // an out-of-range pixel reads (harmlessly) the first input row
-            const uint16_t* rp =
-                ok ? p.A + ((static_cast<int64_t>(img) * p.conv_H + h) * p.conv_W + w) * p.conv_C : p.A;
-            gather8(rp, ok, c0 + j * 8, p.conv_C, v);
-        } else {
-            const bool ok = m < p.M;
-            gather8(p.A + static_cast<int64_t>(ok ? m : 0) * p.lda, ok, c0 + j * 8, p.K, v);
-        }
-    };
-    auto load_b = [&](int idx, uint32_t (&v)[4]) {
-        const int row = idx >> 3, j = idx & 7;
-        const int n = n_row + row;
-        const bool ok = n < p.N;
-        if constexpr (CONV) {
-            const uint16_t* rp =
-                p.B + ((static_cast<int64_t>(ok ? n : 0) * p.conv_R + r) * p.conv_S + sx) * p.conv_C;
-            gather8(rp, ok, c0 + j * 8, p.conv_C, v);
-        } else {
-            gather8(p.B + static_cast<int64_t>(ok ? n : 0) * p.ldb, ok, c0 + j * 8, p.K, v);
-        }
-    };
-    auto store = [&](uint32_t dst, int idx, const uint32_t (&v)[4]) {
-        const int row = idx >> 3, j = idx & 7;
-        st_shared_v4(dst + row * 128 + ((j ^ (row & 7)) << 4), v[0], v[1], v[2], v[3]);
-    };
-    const int li = static_cast<int>(lane);
-#pragma unroll 1
-    for (int base = 0; base < 128 * 8; base += 32 * kBatch) {
-        uint32_t v[kBatch][4];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) load_a(base + i * 32 + li, v[i]);
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) store(dA, base + i * 32 + li, v[i]);
+    for (int q = 0; q < kQuads; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        const uint32_t src = stg + static_cast<uint32_t>(row) * kLdgWindow + 16u * j;
+        lo[q] = 16u * j < end[q] ? ld_shared_v4(src) : make_uint4(0u, 0u, 0u, 0u);
+        hi[q] = 16u * (j + 1u) < end[q] ? ld_shared_v4(src + 16u) : make_uint4(0u, 0u, 0u, 0u);
     }
-#pragma unroll 1
-    for (int base = 0; base < B_ROWS * 8; base += 32 * kBatch) {
-        uint32_t v[kBatch][4];
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) load_b(base + i * 32 + li, v[i]);
+    for (int q = 0; q < kQuads; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        uint32_t c[8] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w, hi[q].x, hi[q].y, hi[q].z, hi[q].w};
+        // drop (mis >> 2) whole words, then shift by (mis & 2) bytes
+        if (mis[q] & 8u) {
 #pragma unroll
-        for (int i = 0; i < kBatch; ++i) store(dB, base + i * 32 + li, v[i]);
+            for (int i = 0; i < 6; ++i) c[i] = c[i + 2];
+        }
+        if (mis[q] & 4u) {
+#pragma unroll
+            for (int i = 0; i < 5; ++i) c[i] = c[i + 1];
+        }
+        const uint32_t sh = (mis[q] & 2u) << 3;  // 0 or 16 bits
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(c[k], c[k + 1], sh);
+        if (!full_k) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // columns 8 j + 2 k and 8 j + 2 k + 1 past the valid range read as zero
+                const int col = static_cast<int>(8u * j) + 2 * k;
+                if (col >= nvalid) o[k] = 0u;
+                else if (col + 1 >= nvalid) o[k] &= 0xFFFFu;
+            }
+        }
+        const int rr = row < 128 ? row : row - 128;
+        const uint32_t dst = (row < 128 ? dA : dB) + static_cast<uint32_t>(rr) * 128u +
+                             ((j ^ (static_cast<uint32_t>(rr) & 7u)) << 4);
+        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -243,8 +343,16 @@ __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, ui
     return ok;
 }
 
+// Threads of a mainloop CTA: producer, MMA issuer, four epilogue warps, and
+// with the plain-load producer three more producer warps.
+template <bool LDG>
+constexpr int mainloop_threads()
+{
+    return LDG ? 192 + 32 * (kLdgWarps - 1) : 192;
+}
+
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapBh,
                     const GemmParams p)
@@ -279,7 +387,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ setup ---
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);   // one arrival: the producer's expect_tx
+            // one arrival: the producer's expect_tx (plain loads: one per producer warp)
+            mbar_init(full_bar(s), LDG ? kLdgWarps : 1);
             mbar_init(empty_bar(s), 1);  // one arrival: the MMA issuer's commit
         }
         for (int b = 0; b < 2; ++b) {
@@ -317,25 +426,63 @@ __global__ void __launch_bounds__(192, 1)
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
-    if (LDG && warp == 0) {
+    if (LDG && (warp == 0 || warp >= 6)) {
         // ------------------------------------- plain-load producer ---
-        int s = 0, it = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
-            const Unit w = unit_of(u, num_tiles, p);
-            int mt, nt;
-            tile_coords(w.tile, p, mt, nt);
-            for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        if constexpr (LDG) {
+            const int pw = warp == 0 ? 0 : warp - 5;  // producer warp 0..kLdgWarps-1 (warps 0, 6, 7, ...)
+            constexpr int RPW = (128 + Cfg::B_ROWS) / kLdgWarps;
+            constexpr uint32_t STG = static_cast<uint32_t>(ldg_staging_buffer_bytes<Cfg::B_ROWS>());
+            static_assert(RPW % 32 == 0, "row quads of 8-apart rows cover whole groups of 32 rows");
+            const uint32_t sStg = sBar + Cfg::BAR_BYTES;
+            // Stage uses in the order the MMA issuer consumes them: (tile rows,
+            // K block). `ahead` is the next use to copy, `cur` the one to unpack.
+            struct Use {
+                int m0, n0, kb;
+            };
+            int ui = cluster_id, kb_next = 0, kb_end = 0;
+            int mt = 0, nt = 0;
+            if (ui < num_units) {
+                const Unit w = unit_of(ui, num_tiles, p);
+                tile_coords(w.tile, p, mt, nt);
+                kb_next = w.kb0;
+                kb_end = w.kb1;
+            }
+            auto fetch = [&](Use& use) -> bool {
+                if (ui >= num_units) return false;
+                use = Use{mt * Cfg::BM, nt * BN, kb_next};
+                if (++kb_next == kb_end) {
+                    ui += num_clusters;
+                    if (ui < num_units) {
+                        const Unit w = unit_of(ui, num_tiles, p);
+                        tile_coords(w.tile, p, mt, nt);
+                        kb_next = w.kb0;
+                        kb_end = w.kb1;
+                    }
+                }
+                return true;
+            };
+            int s = 0, it = 0;
+            uint32_t ph = 0, slot = 0;
+            Use cur{0, 0, 0}, nxt{0, 0, 0};
+            bool have_cur = fetch(cur);
+            if (have_cur)
+                ldg_issue_rows<Cfg::B_ROWS, CONV, RPW>(LdgRows<CONV>(p, cur.m0, cur.n0, cur.kb), sStg, pw, lane);
+            cp_async_commit();
+            while (have_cur) {
+                // copies of the next use go out before this one is unpacked
+                const bool have_nxt = fetch(nxt);
+                if (have_nxt)
+                    ldg_issue_rows<Cfg::B_ROWS, CONV, RPW>(LdgRows<CONV>(p, nxt.m0, nxt.n0, nxt.kb),
+                                                           sStg + (slot ^ 1u) * STG, pw, lane);
+                cp_async_commit();
+                cp_async_wait<1>();  // this use's copies (every lane's, after the warp sync)
+                __syncwarp();
                 int free_ok = 1;
                 if (lane == 0)
                     free_ok = wait_bounded(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
-                if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
-                    ok = false;
-                    break;
-                }
-                ldg_fill_stage<Cfg::B_ROWS, CONV>(p, sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES, mt * Cfg::BM,
-                                                  nt * BN, kb, lane);
+                if (!__shfl_sync(0xffffffffu, free_ok, 0)) break;
+                ldg_repack_rows<Cfg::B_ROWS, RPW>(sStg + slot * STG, LdgRows<CONV>(p, cur.m0, cur.n0, cur.kb).nvalid,
+                                                  sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES, pw, lane);
                 fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
                 __syncwarp();
                 if (lane == 0) {
@@ -347,9 +494,16 @@ __global__ void __launch_bounds__(192, 1)
                     s = 0;
                     ph ^= 1u;
                 }
+                slot ^= 1u;
+                cur = nxt;
+                have_cur = have_nxt;
+                // the staging buffer just unpacked is refilled next iteration;
+                // every lane must be done reading it
+                __syncwarp();
             }
+            cp_async_wait<0>();  // no copy may land after the CTA's shared memory is released
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp == 0) {
         // --------------------------------------------------- producer ---
         if (elect_one()) {
@@ -751,14 +905,15 @@ template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false,
 cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
+    constexpr int SMEM = Cfg::SMEM_BYTES + (LDG ? ldg_staging_bytes<Cfg::B_ROWS>() : 0);
     auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>;
     static std::atomic<uint64_t> smem_set{0};
-    cudaError_t e = smem_limit_once(kern, Cfg::SMEM_BYTES, smem_set);
+    cudaError_t e = smem_limit_once(kern, SMEM, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
-    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.blockDim = dim3(mainloop_threads<LDG>(), 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -777,7 +932,8 @@ constexpr KernelEntry mainloop_entry()
 {
     return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0, SPLITK ? 1 : 0},
                        &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>,
-                       MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES};
+                       MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES +
+                           (LDG ? ldg_staging_bytes<MainloopCfg<CG, BN, STAGES, OUT_F32>::B_ROWS>() : 0)};
 }
 
 }  // namespace tp

@@ -6,10 +6,10 @@
 namespace tp {
 
 static const KernelEntry k_table[] = {
-    mainloop_entry<1, 128, 6, false, false, true>(),
-    mainloop_entry<1, 128, 6, true, false, true>(),
-    mainloop_entry<1, 128, 6, false, true, true>(),
-    mainloop_entry<1, 128, 6, true, true, true>(),
+    mainloop_entry<1, 128, 3, false, false, true>(),
+    mainloop_entry<1, 128, 3, true, false, true>(),
+    mainloop_entry<1, 128, 3, false, true, true>(),
+    mainloop_entry<1, 128, 3, true, true, true>(),
 };
 
 const KernelEntry* table_mainloop_fallback(int* n)

@@ -30,6 +30,7 @@ pytestmark = pytest.mark.gpu
 P = tp.PROTO_PHASES
 S = tp.PROTO_MAX_STAGES
 A_BYTES = 128 * 64 * 2
+LDG_WARPS = 8  # producer warps of the plain-load producer
 
 
 def expected_counts(plan, tma=True):
@@ -53,7 +54,8 @@ def expected_counts(plan, tma=True):
         lead = c * CG
         for s in range(D):
             for k, who in enumerate(bars["full"][0][s].done):
-                exp[lead, s * P + k] = len(who)
+                # the plain-load producer's warps each arrive once per phase
+                exp[lead, s * P + k] = len(who) * (1 if tma else LDG_WARPS)
             for r in range(CG):
                 for k, who in enumerate(bars["empty"][r][s].done):
                     exp[lead + r, (S + s) * P + k] = len(who)
@@ -140,7 +142,8 @@ def test_conv_arrivals_match_the_model(atom, tile_n):
 
 
 def test_plain_load_producer_arrivals_match_the_model():
-    # Odd pitches rule TMA out: one plain arrival per full phase, no bytes.
+    # Odd pitches rule TMA out: one plain arrival per producer warp and full
+    # phase, no bytes.
     M, N, K, ld = 300, 520, 1000, 1001
     A, B = datagen.gemm_operands(M, N, K, seed=112)
     A, B = datagen.pad_rows(A, ld), datagen.pad_rows(B, ld)
