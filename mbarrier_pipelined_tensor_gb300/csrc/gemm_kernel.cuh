@@ -202,30 +202,36 @@ struct LdgRows {
 };
 
 // Issues the cp.async copies of rows [pw * RPW, pw * RPW + RPW) of one stage
-// into staging buffer `stg`: lane j of a row's eight copies aligned chunk j
-// of the 144-byte window that starts at the row's address rounded down to 16
-// bytes (lane 7 also chunk 8), and lane 0 records the row's code: the
+// into staging buffer `stg`. Lane i first works out row pw * RPW + i: the
+// address of its segment rounded down to 16 bytes, and its code -- the
 // window's first valid byte (a & 15) and one past its last (0: row out of
-// range). A chunk is copied only if it holds at least one element of the
-// row's valid range, so no access touches a 16-byte block outside the
-// operand (and none crosses a page).
+// range). The warp's 32 x 9 aligned 16-byte chunks are then copied in nine
+// fully populated instructions, lane i of instruction k taking chunk
+// (32 k + i) mod 9 of row (32 k + i) / 9. A chunk is copied only if it holds
+// at least one element of the row's valid range, so no access touches a
+// 16-byte block outside the operand (and none crosses a page).
 template <int B_ROWS, bool CONV, int RPW>
 __device__ __forceinline__ void ldg_issue_rows(const LdgRows<CONV>& rows, uint32_t stg, int pw, uint32_t lane)
 {
-    const int sub = static_cast<int>(lane >> 3);
-    const uint32_t j = lane & 7u;
+    static_assert(RPW == 32, "one row per lane");
     const uint32_t codes = stg + (128 + B_ROWS) * kLdgWindow;
+    const int myrow = pw * RPW + static_cast<int>(lane);
+    const uintptr_t a = rows.segment(myrow);
+    const uint32_t mis = static_cast<uint32_t>(a & 15u);
+    const uint32_t end = a ? mis + 2u * static_cast<uint32_t>(rows.nvalid) : 0u;
+    st_shared_u32(codes + 4u * static_cast<uint32_t>(myrow), mis | (end << 8));
+    const uint64_t base = static_cast<uint64_t>(a - mis);
+    const uint32_t base_lo = static_cast<uint32_t>(base), base_hi = static_cast<uint32_t>(base >> 32);
+    const uint32_t stg_warp = stg + static_cast<uint32_t>(pw * RPW) * kLdgWindow;
 #pragma unroll
-    for (int q = 0; q < RPW / 4; ++q) {
-        const int row = ldg_row(pw, RPW, q, sub);
-        const uintptr_t a = rows.segment(row);
-        const uint32_t mis = static_cast<uint32_t>(a & 15u);
-        const uint32_t end = a ? mis + 2u * static_cast<uint32_t>(rows.nvalid) : 0u;
-        if (j == 0u) st_shared_u32(codes + 4u * static_cast<uint32_t>(row), mis | (end << 8));
-        const uintptr_t base = a - mis;
-        const uint32_t dst = stg + static_cast<uint32_t>(row) * kLdgWindow;
-        if (16u * j < end) cp_async_16(dst + 16u * j, base + 16u * j);
-        if (j == 7u && 128u < end) cp_async_16(dst + 128u, base + 128u);
+    for (int k = 0; k < kLdgWindow / 16; ++k) {
+        const uint32_t g = 32u * static_cast<uint32_t>(k) + lane;
+        const uint32_t r = g / 9u, ch = g - 9u * r;
+        const uint32_t e = __shfl_sync(0xffffffffu, end, static_cast<int>(r));
+        const uint32_t lo = __shfl_sync(0xffffffffu, base_lo, static_cast<int>(r));
+        const uint32_t hi = __shfl_sync(0xffffffffu, base_hi, static_cast<int>(r));
+        const uint64_t src = (static_cast<uint64_t>(hi) << 32) | lo;
+        if (16u * ch < e) cp_async_16(stg_warp + r * kLdgWindow + 16u * ch, static_cast<uintptr_t>(src + 16u * ch));
     }
 }
 
