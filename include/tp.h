@@ -114,7 +114,7 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               12 pair tiles of the 2-SM atom).
  *   max_ctas:   cap on the persistent grid (0 = one CTA per SM). A cap at
  *               or above the work-unit count (CTAs = units x atom; units =
- *               tiles, plus the narrow tail's extra halves) launches one
+ *               tiles, plus the narrow tail's extra parts) launches one
  *               work unit per cluster, i.e. a non-persistent grid that the
  *               hardware schedules in waves. The narrow tail is sized by the
  *               clusters that run at once: the cap or SMs / atom, whichever
@@ -131,8 +131,9 @@ TP_API int tp_gemm_bf16_f32(const void* A, const void* B, float* C, int64_t M, i
  *               A, read by every tile, stays. It picks 5 in the mirrored
  *               case, else 1.
  *   no_tail:    1 keeps whole tiles in the last wave (the 2-SM, N = 256
- *               variant otherwise runs a partial last wave as half-width
- *               tiles).
+ *               variant otherwise runs a partial last wave of r tiles as
+ *               narrow tiles: 4r quarter-width ones when they fit one wave,
+ *               else 2r half-width ones when those do).
  *   trace:      NULL, or a caller-owned, zeroed device buffer of
  *               TP_TRACE_SLOTS x (CTAs of the launch, tp_plan.grid) uint64
  *               that the mainloop fills with its role timeline (below):
@@ -198,7 +199,7 @@ typedef struct {
 #define TP_TRACE_SLOTS 8
 
 /* Per-unit event timeline per CTA (tp_gemm_opts.events): for the CTA's first
- * TP_EVENT_UNITS work units (output tiles, split-K slices or half-width tail
+ * TP_EVENT_UNITS work units (output tiles, split-K slices or narrow tail
  * units, in the order it runs them), TP_EVENTS_PER_UNIT slots each, in this
  * order: producer about to wait for the unit's first free stage, producer
  * issued the unit's last loads, MMA issuer found the unit's accumulator free,
@@ -423,8 +424,9 @@ typedef struct {
     int smem_bytes;  /* dynamic shared memory per CTA */
     int64_t m_tiles, n_tiles, k_blocks;
     int splits;      /* K slices (1 unless split-K ran) */
-    int tail_units;  /* half-width units of the last wave (0: none) */
+    int tail_units;  /* narrow units of the last wave (0: none) */
     int l2_hint;     /* operand L2 priorities used (tp_gemm_opts.l2_hint 1-6) */
+    int tail_parts;  /* column parts of each narrow-tail tile (2 or 4; 0: no tail) */
 } tp_plan;
 
 /*

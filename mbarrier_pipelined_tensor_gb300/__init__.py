@@ -62,7 +62,7 @@ class tp_plan(ctypes.Structure):
                 ("grid", ctypes.c_int), ("cluster", ctypes.c_int), ("smem_bytes", ctypes.c_int),
                 ("m_tiles", ctypes.c_int64), ("n_tiles", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
                 ("splits", ctypes.c_int), ("tail_units", ctypes.c_int),
-                ("l2_hint", ctypes.c_int)]
+                ("l2_hint", ctypes.c_int), ("tail_parts", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -211,7 +211,8 @@ bool choose_variant(int64_t M, int64_t N, int64_t k_blocks, int sm_count, int ou
         // The 2-SM, N = 256 variant runs a partial last wave that fits twice
         // as half-width units: after at least one full wave it counts half.
         const int64_t r = tiles % clusters;
-        if (c.atom == 2 && c.tile_n == 256 && tiles >= clusters && r > 0 && 2 * r <= clusters) waves -= 0.5;
+        if (c.atom == 2 && c.tile_n == 256 && tiles >= clusters && r > 0 && 2 * r <= clusters)
+            waves -= 4 * r <= clusters ? 0.6 : 0.5;
         // Estimated time (ns): one k-block of a 128 x tile_n tile is 1.31 *
         // tile_n ns at one SM's dense BF16 rate, scaled by the variant's
         // measured efficiency.
@@ -316,14 +317,20 @@ int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom);
 // partial wave (r = tiles mod W) fit twice into one wave, they run as 2r
 // half-width units, so that wave takes about half as long. W is the number
 // of clusters that run at once: the grid cap (max_ctas) or the GPU's SMs /
-// 2, whichever is smaller. A problem with fewer tiles than W is all tail:
-// its tiles run as half-width units on twice as many clusters. The grid is
-// W clusters (persistent), or one per unit when the cap allows as many
-// (non-persistent).
+// 2, whichever is smaller. When they fit four times into one wave they run
+// as 4r quarter-width units instead (N = 64): the tail is bound by each
+// CTA's operand stream, which a quarter unit cuts by a sixth against a half
+// (A 16 KiB + B 4 KiB against 16 + 8 per K block) while it also halves the
+// MMAs; the conv 32x56x56x256 (12 tiles left on 76 clusters) ran its tail
+// in 5.6 instead of 6.7 us. A problem with fewer tiles than W is all tail.
+// The grid is W clusters (persistent), or one per unit when the cap allows
+// as many (non-persistent).
 void set_narrow_tail(tp_plan& pl, GemmParams& p, const tp_gemm_opts* o, int sm_count)
 {
     p.n_full = 0;
     p.tail_units = 0;
+    p.tail_parts = 2;
+    pl.tail_parts = 0;
     if (pl.atom != 2 || pl.tile_n != 256) return;
     const int64_t cap = max_clusters_for(o, sm_count, pl.atom);
     const int64_t wave = std::min<int64_t>(cap, std::max<int64_t>(1, sm_count / pl.atom));
@@ -331,11 +338,14 @@ void set_narrow_tail(tp_plan& pl, GemmParams& p, const tp_gemm_opts* o, int sm_c
     const int64_t tiles = pl.m_tiles * pl.n_tiles;
     const int64_t r = tiles % wave;
     if (r == 0 || 2 * r > wave) return;
+    const int parts = 4 * r <= wave ? 4 : 2;
     p.n_full = static_cast<int>(tiles - r);
-    p.tail_units = static_cast<int>(2 * r);
-    const int64_t units = tiles - r + 2 * r;
+    p.tail_units = static_cast<int>(parts * r);
+    p.tail_parts = parts;
+    const int64_t units = tiles - r + parts * r;
     pl.grid = static_cast<int>(std::min<int64_t>(cap, units) * pl.atom);
     pl.tail_units = p.tail_units;
+    pl.tail_parts = parts;
 }
 
 int64_t max_clusters_for(const tp_gemm_opts* o, int sm_count, int atom)
@@ -576,6 +586,9 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     const int b_rows = pl.tile_n / cg;
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
+    GemmParams& p = L.params;
+    // the narrow tail (2-SM, N = 256) before the maps: it sets their box
+    if (!use_splitk && !(opts && opts->no_tail)) set_narrow_tail(pl, p, opts, dev->sm_count);
     const uint32_t eb = out_f32 ? 4 : 2;
     // TMA stores write whole 16-byte granules of a row: the C map ends at the
     // last full granule, the epilogue stores the rest (all of C when the
@@ -592,10 +605,10 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
                      {64, static_cast<uint32_t>(b_rows)}, CU_TENSOR_MAP_SWIZZLE_128B};
         if ((st = encode_tiled(&L.mapA, da)) || (st = encode_tiled(&L.mapB, db))) return st;
         L.mapBh = L.mapB;
-        if (pl.atom == 2 && pl.tile_n == 256 && !use_splitk) {
-            // the narrow tail's half-width units: half of each CTA's B rows
+        if (p.tail_units > 0) {
+            // the narrow tail's units: a half or a quarter of each CTA's B rows
             TiledDesc dbh = db;
-            dbh.box[1] = static_cast<uint32_t>(b_rows / 2);
+            dbh.box[1] = static_cast<uint32_t>(b_rows / p.tail_parts);
             if ((st = encode_tiled(&L.mapBh, dbh))) return st;
         }
         if (use_splitk) {
@@ -615,7 +628,6 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
             L.mapC = L.mapA;
         }
     }
-    GemmParams& p = L.params;
     p.A = static_cast<const uint16_t*>(A);
     p.B = static_cast<const uint16_t*>(B);
     p.lda = lda;
@@ -628,8 +640,6 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.k_blocks = static_cast<int>(pl.k_blocks);
     p.splits = use_splitk ? pl.splits : 1;
     p.kb_per_split = use_splitk ? kps : p.k_blocks;
-    if (!use_splitk && !(opts && opts->no_tail))
-        set_narrow_tail(pl, p, opts, dev->sm_count);
     p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);
     p.n_tma = static_cast<int>(n_tma);
@@ -742,6 +752,9 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     const int b_rows = pl.tile_n / cg;
     GemmLaunch L;
     std::memset(&L, 0, sizeof(L));
+    GemmParams& p = L.params;
+    // the narrow tail (2-SM, N = 256) before the maps: it sets their box
+    if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, opts, dev->sm_count);
     if (!ldg) {
         Im2colDesc dx{};
         dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -777,9 +790,9 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
                      {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
         if ((st = encode_im2col(&L.mapA, dx)) || (st = encode_tiled(&L.mapB, dw))) return st;
         L.mapBh = L.mapB;
-        if (pl.atom == 2 && pl.tile_n == 256) {
+        if (p.tail_units > 0) {
             TiledDesc dwh = dw;
-            dwh.box[2] = static_cast<uint32_t>(b_rows / 2);
+            dwh.box[2] = static_cast<uint32_t>(b_rows / p.tail_parts);
             if ((st = encode_tiled(&L.mapBh, dwh))) return st;
         }
         if (y_tma) {
@@ -788,7 +801,6 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
             L.mapC = L.mapB;  // never stored through (n_tma = 0)
         }
     }
-    GemmParams& p = L.params;
     p.A = static_cast<const uint16_t*>(x);
     p.B = static_cast<const uint16_t*>(w);
     p.conv_H = static_cast<int>(H);
@@ -803,7 +815,6 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.k_blocks = static_cast<int>(pl.k_blocks);
     p.splits = 1;
     p.kb_per_split = p.k_blocks;
-    if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, opts, dev->sm_count);
     p.group_m = group_m_for(opts, pl.m_tiles, pl.atom);
     pl.l2_hint = l2_mode_for(opts, pl.m_tiles, pl.n_tiles, 0.0, 0.0, false);
     l2_hints_for(pl.l2_hint, &p.l2_a, &p.l2_b);

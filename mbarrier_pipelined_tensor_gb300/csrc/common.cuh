@@ -107,9 +107,10 @@ struct GemmParams {
     // workspace C map. splits == 1 is the plain GEMM.
     int splits, kb_per_split;
     // Narrow tail (2-SM atom, splits == 1): units [0, n_full) are whole
-    // tiles; the last tail_units units are half-width tiles (N = BN/2), two
-    // per remaining tile, so the last, partial wave takes about half as long.
-    int n_full, tail_units;
+    // tiles; the last tail_units units are narrow tiles (N = BN / tail_parts,
+    // tail_parts of 2 or 4 per remaining tile), so the last, partial wave
+    // takes about a half or a quarter as long.
+    int n_full, tail_units, tail_parts;
     int group_m;   // tile raster: group_m M-tiles share a sweep over N
     int l2_a, l2_b;  // L2 eviction priority of A / B loads (0 normal, 1 first, 2 last)
     // convolution only
@@ -244,7 +245,7 @@ struct KernelKey {
 
 struct GemmLaunch {
     CUtensorMap mapA, mapB, mapC;
-    CUtensorMap mapBh;  // B with half-height boxes: the 2-SM, N = 256 narrow tail
+    CUtensorMap mapBh;  // B with narrow boxes (half or quarter height): the 2-SM, N = 256 narrow tail
     GemmParams params;
     int grid;
     cudaStream_t stream;

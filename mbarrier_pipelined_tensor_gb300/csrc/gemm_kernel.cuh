@@ -59,9 +59,11 @@ struct MainloopCfg {
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * CG;  // the leader's expect_tx covers the pair
-    // A half-width unit (the 2-SM, N = 256 narrow tail) loads half of each
-    // CTA's B rows through a half-height box.
+    // A narrow unit (the 2-SM, N = 256 narrow tail: a half or a quarter of a
+    // tile's columns) loads that share of each CTA's B rows through a box of
+    // that height.
     static constexpr int TX_HALF_BYTES = (A_BYTES + B_BYTES / 2) * CG;
+    static constexpr int TX_QUARTER_BYTES = (A_BYTES + B_BYTES / 4) * CG;
     static constexpr int OUT_BYTES = OUT_F32 ? 4 : 2;
     static constexpr int EPI_COLS = 128 / OUT_BYTES;  // columns per 128-byte staging row
     static constexpr int EPI_WARPS = 4;
@@ -299,10 +301,11 @@ __device__ __forceinline__ void ldg_repack_rows(uint32_t stg, int nvalid, uint32
     }
 }
 
-// Work unit u of a launch: output tile, its K-block range, and which half
-// of the tile's columns it covers (-1: the whole tile).
+// Work unit u of a launch: output tile, its K-block range, and which part
+// of the tile's columns it covers (-1: the whole tile; else one of
+// p.tail_parts equal column parts of a narrow-tail tile).
 struct Unit {
-    int tile, split, kb0, kb1, half;
+    int tile, split, kb0, kb1, part;
 };
 
 __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& p)
@@ -310,8 +313,8 @@ __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& 
     Unit w;
     if (p.tail_units > 0 && u >= p.n_full) {
         const int v = u - p.n_full;
-        w.tile = p.n_full + (v >> 1);
-        w.half = v & 1;
+        w.tile = p.n_full + v / p.tail_parts;
+        w.part = v - (w.tile - p.n_full) * p.tail_parts;
         w.split = 0;
         w.kb0 = 0;
         w.kb1 = p.k_blocks;
@@ -321,7 +324,7 @@ __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& 
     w.tile = u - w.split * num_tiles;
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
-    w.half = -1;
+    w.part = -1;
     return w;
 }
 
@@ -540,13 +543,17 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
                     int mt, nt;
                     tile_coords(w.tile, p, mt, nt);
                     const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM;
-                    // A half-width unit (2-SM only) needs BN/4 rows of B per CTA,
-                    // starting at its half; the B box (BN/2 rows) loads them first.
-                    const int n_row = w.half < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
-                                                 : nt * BN + w.half * (BN / 2) + static_cast<int>(rank) * (BN / 4);
-                    // half-width units (2-SM, N = 256 only) load B through the half-height box
-                    const bool hu = CG == 2 && BN == 256 && w.half >= 0;
+                    // A narrow unit (2-SM only) of the tile's p.tail_parts column
+                    // parts needs BN / (2 parts) rows of B per CTA, starting at
+                    // its part; the narrow box loads just them.
+                    const int pw = BN / p.tail_parts;  // columns of a narrow unit
+                    const int n_row = w.part < 0 ? nt * BN + static_cast<int>(rank) * Cfg::B_ROWS
+                                                 : nt * BN + w.part * pw + static_cast<int>(rank) * (pw / 2);
+                    // narrow units (2-SM, N = 256 only) load B through the narrow box
+                    const bool hu = CG == 2 && BN == 256 && w.part >= 0;
                     const CUtensorMap* const mB = hu ? &mapBh : &mapB;
+                    const uint32_t tx = !hu ? Cfg::TX_BYTES
+                                            : (p.tail_parts == 4 ? Cfg::TX_QUARTER_BYTES : Cfg::TX_HALF_BYTES);
                     // GEMM units of odd waves walk K backwards: the clusters
                     // of one wave share A rows with the wave before, whose
                     // last K blocks are the ones still in L2.
@@ -571,17 +578,17 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
                             break;
                         }
                         const uint32_t fb = fb0 + 8u * static_cast<uint32_t>(s);
-                        if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), hu ? Cfg::TX_HALF_BYTES : Cfg::TX_BYTES);
+                        if (leader && arrive) mbar_arrive_expect_tx(full_bar(s), tx);
                         if constexpr (PR) {
                             // phase issued / STAGES of stage s, on the leader's barrier
                             const int lead = static_cast<int>(blockIdx.x) - static_cast<int>(rank);
                             const int k = issued / STAGES;
                             if (leader && arrive) {
                                 proto_add(p.proto, lead, PROTO_BAR_FULL, s, k, 1);
-                                proto_add(p.proto, lead, PROTO_ROW_TX_EXPECT, s, k, hu ? Cfg::TX_HALF_BYTES : Cfg::TX_BYTES);
+                                proto_add(p.proto, lead, PROTO_ROW_TX_EXPECT, s, k, tx);
                             }
                             proto_add(p.proto, lead, PROTO_ROW_TX_ISSUED, s, k,
-                                      Cfg::A_BYTES + (hu ? Cfg::B_BYTES / 2 : Cfg::B_BYTES));
+                                      Cfg::A_BYTES + (hu ? Cfg::B_BYTES / p.tail_parts : Cfg::B_BYTES));
                         }
                         arrive = true;
                         const uint32_t dA = sA + s * Cfg::A_BYTES;
@@ -677,6 +684,8 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
             if (elect_one()) {
                 constexpr uint32_t IDESC = umma_idesc_bf16_f32(Cfg::BM * CG, BN);
                 constexpr uint32_t IDESC_HALF = umma_idesc_bf16_f32(Cfg::BM * CG, BN / 2);
+                constexpr uint32_t IDESC_QUARTER = umma_idesc_bf16_f32(Cfg::BM * CG, BN / 4 >= 16 * CG ? BN / 4 : BN / 2);
+                const uint32_t idesc_narrow = p.tail_parts == 4 ? IDESC_QUARTER : IDESC_HALF;
                 int s = 0;
                 uint32_t ph = 0;
                 int lt = 0;
@@ -709,7 +718,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
                         if (p.events) event_at(p, lt, EV_MMA_START, globaltimer_ns());
                         tcgen05_fence_after();
                         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-                        const uint32_t idesc = w.half < 0 ? IDESC : IDESC_HALF;
+                        const uint32_t idesc = w.part < 0 ? IDESC : idesc_narrow;
                         uint32_t accumulate = 0;  // the unit's first MMA overwrites the accumulator
                         for (int kb = w.kb0; kb < w.kb1; ++kb) {
                             if (!timed_wait(p, full_bar(s), ph, abort_flag, SITE_MMA_FULL, t_full)) {
@@ -789,8 +798,8 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
             int mt, nt;
             tile_coords(w.tile, p, mt, nt);
             const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM + quarter * 32;
-            const int n0 = nt * BN + (w.half < 0 ? 0 : w.half * (BN / 2));
-            const int max_chunks = w.half < 0 ? CHUNKS : CHUNKS / 2;
+            const int n0 = nt * BN + (w.part < 0 ? 0 : w.part * (BN / p.tail_parts));
+            const int max_chunks = w.part < 0 ? CHUNKS : CHUNKS / p.tail_parts;
             int nchunks = 0;
             if (m_row < p.M && n0 < p.N) {
                 nchunks = (p.N - n0 + Cfg::EPI_COLS - 1) / Cfg::EPI_COLS;

@@ -78,16 +78,22 @@ def test_atom2_conv(tile_n, out_f32):
 # ------------------------------------------------------ narrow tail ---
 
 @pytest.mark.parametrize("M,N,K,max_ctas", [(1280, 512, 640, 8),     # 10 tiles on 4 clusters: 8 whole + 4 halves
-                                             (2560, 2048, 384, 0),    # 80 tiles on 76 clusters: 76 + 8 halves
-                                             (2560, 2048, 384, 100000),  # the same, one cluster per unit (84)
-                                             (600, 100, 448, 0),      # 3 tiles, all halves; upper halves out of N
-                                             (320, 200, 448, 0)])
+                                             (2560, 2048, 384, 0),    # 80 tiles on 76 clusters: 76 + 16 quarters
+                                             (2560, 2048, 384, 100000),  # the same, one cluster per unit (92)
+                                             (600, 100, 448, 0),      # 3 tiles, all quarters; upper ones out of N
+                                             (320, 200, 448, 0),
+                                             (5120, 4096, 448, 0)])   # 320 tiles on 76: 304 whole + 32 halves
 @pytest.mark.parametrize("out_f32", [True, False])
 def test_narrow_tail_units(M, N, K, max_ctas, out_f32):
     A, B = datagen.gemm_operands(M, N, K, seed=M + N)
     ldc = (N + 7) // 8 * 8
     got, plan = run_gemm(A, B, M, N, K, K, K, ldc=ldc, out_f32=out_f32, atom=2, tile_n=256, max_ctas=max_ctas)
-    assert plan["tail_units"] > 0
+    assert plan["tail_units"] > 0 and plan["tail_parts"] in (2, 4)
+    tiles = plan["m_tiles"] * plan["n_tiles"]
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    wave = min(pairs, max_ctas // 2) if max_ctas else pairs   # clusters that run at once
+    r = tiles % wave
+    assert plan["tail_parts"] == (4 if 4 * r <= wave else 2)  # quarters when they fit one wave
     ref, ab = oracle.gemm(A, B, M, N, K, K, K)
     check_against_oracle(got, ref, ab, out_f32, f"narrow tail {M}x{N}x{K}")
     got2, plan2 = run_gemm(A, B, M, N, K, K, K, ldc=ldc, out_f32=out_f32, atom=2, tile_n=256, max_ctas=max_ctas,
@@ -99,12 +105,12 @@ def test_narrow_tail_units(M, N, K, max_ctas, out_f32):
 
 
 def test_narrow_tail_conv():
-    N, H, W, C, K, R, S = 4, 20, 18, 64, 256, 3, 3   # 1440 pixels: 6 pair tiles, all halves
+    N, H, W, C, K, R, S = 4, 20, 18, 64, 256, 3, 3   # 1440 pixels: 6 pair tiles, all quarters
     x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=23)
     y = new_out(N * H * W, K, False)
     tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, 1, 1, atom=2, tile_n=256)
     expect_ok()
-    assert tp.tp_last_plan()["tail_units"] == 12
+    assert tp.tp_last_plan()["tail_units"] == 24 and tp.tp_last_plan()["tail_parts"] == 4
     ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, 1)
     check_against_oracle(host_f64(y), ref, ab, False, "conv narrow tail")
 
@@ -126,7 +132,9 @@ def test_role_timeline(atom, tile_n):
     t = trace.view(plan["grid"], tp.TRACE_SLOTS).cpu().numpy()
     issuers = t[::atom]                                         # the pair's leader issues the MMAs
     tiles = plan["m_tiles"] * plan["n_tiles"]
-    assert issuers[:, 7].sum() == tiles + plan["tail_units"] // 2  # whole tiles, plus 2 units per tail tile
+    parts = plan["tail_parts"] or 1
+    # whole tiles, with each tail tile split into `parts` units
+    assert issuers[:, 7].sum() == tiles - plan["tail_units"] // parts + plan["tail_units"]
     for rows, span, wait in ((t, 0, 1), (issuers, 2, 3), (issuers, 2, 4), (t, 5, 6)):
         assert np.all(rows[:, span] > 0) and np.all(rows[:, wait] <= rows[:, span])
 
@@ -153,7 +161,8 @@ def test_event_timeline(atom, tile_n):
     e = ev.view(grid, tp.EVENT_UNITS, tp.EVENTS_PER_UNIT).cpu().numpy().astype(np.int64)
     P0, P1, M0, M1, E0, E1, E2, U = range(8)
     clusters = grid // atom
-    units = plan["m_tiles"] * plan["n_tiles"] + plan["tail_units"] // 2
+    parts = plan["tail_parts"] or 1
+    units = plan["m_tiles"] * plan["n_tiles"] - plan["tail_units"] // parts + plan["tail_units"]
     assert units >= clusters * tp.EVENT_UNITS   # every CTA fills all its event slots
     for cta in range(grid):
         cid, leader = cta // atom, cta - (cta // atom) * atom == 0

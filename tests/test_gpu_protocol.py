@@ -39,7 +39,8 @@ def expected_counts(plan, tma=True):
     CG, D, grid, KB = plan["cluster"], plan["pipe_depth"], plan["grid"], plan["k_blocks"]
     tiles = plan["m_tiles"] * plan["n_tiles"]
     tail = plan["tail_units"]
-    n_full = tiles - tail // 2 if tail else tiles
+    parts = plan["tail_parts"] or 1
+    n_full = tiles - tail // parts if tail else tiles
     num_units = n_full + tail if tail else tiles
     clusters = grid // CG
     b_bytes = plan["tile_n"] // CG * 64 * 2
@@ -68,8 +69,8 @@ def expected_counts(plan, tma=True):
         if tma:
             for it in range(len(units) * KB):
                 s, k = it % D, it // D
-                half = tail > 0 and units[it // KB] >= n_full
-                nbytes = CG * (A_BYTES + (b_bytes // 2 if half else b_bytes))
+                narrow = tail > 0 and units[it // KB] >= n_full
+                nbytes = CG * (A_BYTES + (b_bytes // parts if narrow else b_bytes))
                 exp[lead, tp.PROTO_TX_EXPECT + s * P + k] = nbytes
                 exp[lead, tp.PROTO_TX_ISSUED + s * P + k] = nbytes
     return exp
@@ -96,14 +97,15 @@ def counted(launch):
 
 
 GEMM_VARIANTS = [(1, 128, 2, 4), (1, 128, 6, 4), (1, 64, 8, 4), (1, 256, 4, 4), (2, 128, 2, 4), (2, 128, 6, 4),
-                 (2, 128, 8, 4), (2, 256, 2, 8), (2, 256, 6, 8)]
+                 (2, 128, 8, 4), (2, 256, 2, 8), (2, 256, 6, 8), (2, 256, 6, 0)]
 
 
 @pytest.mark.parametrize("atom,tile_n,depth,ctas", GEMM_VARIANTS)
 def test_gemm_arrivals_match_the_model(atom, tile_n, depth, ctas):
     # Ragged M, N and K (16 k-blocks, the last 40 deep); a small grid so that
     # each CTA runs several units and wraps the ring many times. The 2-SM,
-    # N = 256 cases (6 pair tiles on 4 clusters) end in half-width units.
+    # N = 256 cases end in narrow units: 6 pair tiles on 4 clusters in
+    # halves, on the whole GPU in quarters.
     M, N, K = 300, 520, 1000
     A, B = datagen.gemm_operands(M, N, K, seed=110)
     a, b = dev_bf16(A), dev_bf16(B)

@@ -228,9 +228,9 @@ def test_splitk_workspace_arithmetic():
 
 def test_narrow_tail_plan():
     # 8192^3 on 152 SMs: 1024 pair tiles, 76 clusters, 36 left for the last
-    # wave -> 72 half-width units.
+    # wave -> 72 half-width units (144 quarters would not fit one wave).
     st, p = plan(8192, 8192, 8192)
-    assert (p["atom"], p["tile_n"], p["tail_units"], p["grid"]) == (2, 256, 72, 152)
+    assert (p["atom"], p["tile_n"], p["tail_units"], p["tail_parts"], p["grid"]) == (2, 256, 72, 2, 152)
     st, p = plan(8192, 8192, 8192, no_tail=1)
     assert p["tail_units"] == 0
     # A grid cap above the machine (non-persistent launch): the wave is still
@@ -238,13 +238,15 @@ def test_narrow_tail_plan():
     # and each of the 988 + 72 units gets a cluster of its own.
     st, p = plan(8192, 8192, 8192, atom=2, tile_n=256, max_ctas=100000)
     assert (p["tail_units"], p["grid"]) == (72, 2 * 1060)
-    st, p = plan(100352, 256, 2304, atom=2, tile_n=256, max_ctas=100000)   # 392 tiles: 5 waves + 12
-    assert (p["tail_units"], p["grid"]) == (24, 2 * 404)
+    # The conv's GEMM view, 392 tiles: 5 waves + 12, and 4 x 12 <= 76 -> 48
+    # quarter-width units.
+    st, p = plan(100352, 256, 2304, atom=2, tile_n=256, max_ctas=100000)
+    assert (p["tail_units"], p["tail_parts"], p["grid"]) == (48, 4, 2 * 428)
     st, p = plan(100352, 256, 2304, atom=2, tile_n=256)
-    assert (p["tail_units"], p["grid"]) == (24, 152)
-    # 10 tiles on 4 clusters: 8 whole, 2 left -> 4 halves.
+    assert (p["tail_units"], p["tail_parts"], p["grid"]) == (48, 4, 152)
+    # 10 tiles on 4 clusters: 8 whole, 2 left -> 4 halves (8 quarters would not fit).
     st, p = plan(1280, 512, 640, atom=2, tile_n=256, max_ctas=8)
-    assert (p["tail_units"], p["grid"]) == (4, 8)
+    assert (p["tail_units"], p["tail_parts"], p["grid"]) == (4, 2, 8)
     # No tail when the leftover does not fit twice into a wave, or for N = 128.
     st, p = plan(2048 * 5, 256 * 16, 512, atom=2, tile_n=256)     # 40 x 16 = 640 tiles: 640 % 76 = 32 fits
     assert p["tail_units"] == 64

@@ -77,15 +77,21 @@ def test_plans_satisfy_invariants(compiled):
         tiles = p["m_tiles"] * p["n_tiles"]
         cap = opts.get("max_ctas", SM_COUNT)
         clusters = p["grid"] // p["atom"]
-        assert 1 <= clusters <= max(1, cap // p["atom"]) or (p["tail_units"] and clusters <= 2 * tiles)
-        units = tiles if not p["tail_units"] else tiles + p["tail_units"] // 2
+        parts = p["tail_parts"]
+        assert 1 <= clusters <= max(1, cap // p["atom"]) or (p["tail_units"] and clusters <= parts * tiles)
+        units = tiles if not p["tail_units"] else tiles - p["tail_units"] // parts + p["tail_units"]
         assert clusters <= units
         if p["tail_units"]:
             # Narrow tail: only the 2-SM, N = 256 variant, never with no_tail,
-            # two half-width units per leftover tile, at most one wave of them.
+            # two or four narrow units per leftover tile, at most one wave of
+            # them, quarters whenever they fit.
             assert (p["atom"], p["tile_n"]) == (2, 256) and not opts.get("no_tail")
-            assert p["tail_units"] % 2 == 0 and p["tail_units"] // 2 <= tiles
-            assert p["tail_units"] <= max(clusters, 2)
+            assert parts in (2, 4) and p["tail_units"] % parts == 0 and p["tail_units"] // parts <= tiles
+            assert p["tail_units"] <= max(clusters, parts)
+            wave = min(max(1, cap // 2), SM_COUNT // 2)
+            assert (parts == 4) == (4 * (p["tail_units"] // parts) <= wave)
+        else:
+            assert parts == 0
         assert p["l2_hint"] in range(1, 7)
     assert checked > 1000
 
