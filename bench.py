@@ -56,8 +56,11 @@ def parse_args():
     ap.add_argument("--size", type=int, default=8192, help="M = N = K of the timed GEMM")
     ap.add_argument("--group-m", type=int, default=0, help="tile raster group (0 = library default)")
     ap.add_argument("--l2-hint", type=int, default=0, help="operand L2 priorities (tp_gemm_opts.l2_hint)")
-    ap.add_argument("--only", choices=["conv", "copy", "transpose"], default=None,
+    ap.add_argument("--only", choices=["gemm", "conv", "copy", "transpose"], default=None,
                     help="time only this workload for --steps launches (for profiling)")
+    ap.add_argument("--shape", type=str, default="", help="M,N,K for --only gemm (default: --size cubed)")
+    ap.add_argument("--pitch", type=int, default=0,
+                    help="row pitch of A and B in elements for --only gemm (0 = K, the packed layout)")
     ap.add_argument("--conv-n", type=int, default=32, help="conv batch for --only conv")
     ap.add_argument("--copy-rows", type=int, default=32768, help="rows (x 16384) for --only copy/transpose")
     ap.add_argument("--gsweep", type=str, default="",
@@ -777,7 +780,25 @@ def only_arm(args):
     import mbarrier_pipelined_tensor_gb300 as tp
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
-    if args.only == "conv":
+    if args.only == "gemm":
+        M, N, K = (int(v) for v in args.shape.split(",")) if args.shape else (args.size,) * 3
+        ld = args.pitch or K
+        if ld < K:
+            raise SystemExit("--pitch must be at least K")
+        A, B = datagen.gemm_operands(M, N, K, seed=3, lda=ld, ldb=ld)
+        a = torch.from_numpy(A.view(np.int16)).cuda().view(torch.bfloat16)
+        b = torch.from_numpy(B.view(np.int16)).cuda().view(torch.bfloat16)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        o = {k: v for k, v in (("atom", args.atom), ("tile_n", args.tile_n), ("pipe_depth", args.depth)) if v}
+        gemm = lambda: tp.tp_gemm_bf16_ex(a, b, c, M, N, K, ld, ld, N, stream=s, **o)  # noqa: E731
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+        def fn():
+            flush.fill_(1)     # every launch starts from operands in HBM, as in the bench rows
+            gemm()
+        work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s (flush included)"
+        workload = f"gemm {M}x{N}x{K} lda=ldb={ld}"
+    elif args.only == "conv":
         N, H, W, C, K, R, S = args.conv_n, 56, 56, 256, 256, 3, 3
         x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=2)
         xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)

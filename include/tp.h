@@ -80,8 +80,11 @@ enum {
  *      (no alpha/beta). K == 0 writes zeros.
  * The TMA producer needs A, B, C 16-byte aligned and lda*2, ldb*2, ldc*2
  * multiples of 16; other layouts take the plain-load producer (1-SM atom,
- * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED),
- * which is correct but about 50x slower on a large GEMM.
+ * N = 128; atom / tile_n choices other than those return TP_ERR_UNSUPPORTED).
+ * It loads each row class (rows r mod 8, which sit a multiple of 16 bytes
+ * apart) through its own TMA window and shifts the rows into place in
+ * shared memory: about a quarter of the TMA producer's rate on a large
+ * GEMM. C is still written with TMA stores when it is aligned.
  * Repeating a call gives the same bits. The fp32 summation order of a tile
  * depends on the variant and on the wave the tile runs in (a persistent
  * CTA's odd-numbered tiles take their K blocks last to first), so calls

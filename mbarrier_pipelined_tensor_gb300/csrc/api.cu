@@ -156,13 +156,16 @@ const KernelEntry* find_kernel(const KernelKey& k)
 }
 
 // Mirrors MainloopCfg::SMEM_BYTES (plus, for the plain-load producer, its
-// staging buffers).
-int64_t mainloop_smem(int atom, int depth, int tile_n, int ldg = 0)
+// staging buffers: ldg_extra_bytes).
+int64_t mainloop_smem(int atom, int depth, int tile_n, int ldg = 0, int conv = 0)
 {
     const int64_t a = 128 * 64 * 2;
+    const int64_t rows = 128 + tile_n / atom;
     const int64_t b = static_cast<int64_t>(tile_n / atom) * 64 * 2;
     const int64_t epi = 4 * 2 * 32 * 128;
-    const int64_t staging = ldg ? static_cast<int64_t>(kLdgStaging) * (128 + tile_n / atom) * kLdgWindow : 0;
+    const int64_t staging = !ldg ? 0
+                            : conv ? static_cast<int64_t>(kLdgStaging) * rows * (kLdgWindow + 4)
+                                   : static_cast<int64_t>(kWinStaging) * rows * kWinRow + 64;
     return 1024 + depth * (a + b) + epi + 256 + staging;
 }
 
@@ -253,10 +256,12 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
         !choose_variant(M, N, k_blocks, sm_count, out_f32, conv, splitk, &atom, &tile_n))
         return TP_ERR_UNSUPPORTED;
     // The plain-load producer stages its copies outside the ring, which
-    // leaves room for kLdgStages ring stages.
-    int depth = o && o->pipe_depth ? o->pipe_depth : (ldg ? kLdgStages : deepest_fitting(atom, tile_n));
+    // leaves room for kLdgStages ring stages (the GEMM's row-class windows:
+    // kWinStages).
+    int depth = o && o->pipe_depth ? o->pipe_depth
+                                   : (ldg ? (conv ? kLdgStages : kWinStages) : deepest_fitting(atom, tile_n));
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
-    const int64_t smem = mainloop_smem(atom, depth, tile_n, ldg);
+    const int64_t smem = mainloop_smem(atom, depth, tile_n, ldg, conv);
     if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
     const KernelEntry* k = find_kernel(KernelKey{atom, tile_n, depth, out_f32, conv, ldg, 0});
     if (!k) return TP_ERR_UNSUPPORTED;
@@ -400,6 +405,32 @@ void l2_hints_for(int mode, int* a, int* b)
     case 7: *a = 3; *b = 3; break;
     default: break;  // 1: normal priority, no policy
     }
+}
+
+// Row-class windows (WinMaps) of a bf16 operand of `rows` rows of K
+// elements at pitch ld (elements; any base with 2-byte alignment): class
+// q's map starts at row q's address rounded down to 16 bytes, steps 8 rows
+// (16 ld bytes) per row, and is K plus the rounding (delta, in elements)
+// wide, so TMA reads nothing outside the operand and fills past K with
+// zeros. A class with no rows (rows < 8) repeats class 0: the tile rows it
+// feeds lie past the last row and are never stored.
+int encode_windows(CUtensorMap* maps, const void* X, int64_t K, int64_t rows, int64_t ld, uint32_t box_rows,
+                   uint32_t* deltas)
+{
+    *deltas = 0;
+    for (int q = 0; q < 8; ++q) {
+        const int64_t c = q < rows ? q : 0;
+        const uintptr_t row = reinterpret_cast<uintptr_t>(X) + static_cast<uintptr_t>(c * ld * 2);
+        const uintptr_t base = row & ~static_cast<uintptr_t>(15);
+        const uint32_t delta = static_cast<uint32_t>((row - base) / 2);
+        TiledDesc d{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void*>(base),
+                    {static_cast<uint64_t>(K + delta), static_cast<uint64_t>((rows - c + 7) / 8)},
+                    {static_cast<uint64_t>(ld) * 16}, {72, box_rows}, CU_TENSOR_MAP_SWIZZLE_NONE};
+        const int st = encode_tiled(&maps[q], d);
+        if (st) return st;
+        *deltas |= delta << (3 * q);
+    }
+    return TP_OK;
 }
 
 int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -595,8 +626,19 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     // plain-load path runs). Split-K partials go to the workspace, whose rows
     // are whole granules.
     const bool c_tma = aligned16(C) && (ldc * eb) % 16 == 0;
-    const int64_t n_tma = use_splitk ? ldw : (ldg || !c_tma ? 0 : N / (16 / eb) * (16 / eb));
-    if (!ldg) {
+    const int64_t n_tma = use_splitk ? ldw : (!c_tma ? 0 : N / (16 / eb) * (16 / eb));
+    if (ldg) {
+        // the plain-load GEMM: row-class windows of A and B, and C's map
+        if ((st = encode_windows(L.win.a, A, K, M, lda, 16, &p.win_delta_a)) ||
+            (st = encode_windows(L.win.b, B, K, N, ldb, static_cast<uint32_t>(b_rows / 8), &p.win_delta_b)))
+            return st;
+        if (c_tma) {
+            TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
+                         {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
+                         {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+            if ((st = encode_tiled(&L.mapC, dc))) return st;
+        }
+    } else {
         TiledDesc da{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A),
                      {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(lda) * 2},
                      {64, 128}, CU_TENSOR_MAP_SWIZZLE_128B};

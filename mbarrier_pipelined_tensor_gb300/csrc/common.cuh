@@ -121,6 +121,10 @@ struct GemmParams {
     const uint16_t* B;
     int64_t lda, ldb;
     int conv_H, conv_W, conv_C, conv_R;
+    // plain-load GEMM (row-class windows, below): element offset (0..7) of
+    // row class q's rows inside their 16-byte-aligned windows, 3 bits per
+    // class, for A and B
+    uint32_t win_delta_a, win_delta_b;
     // Optional role timeline: kTraceSlots counters per CTA (nanoseconds,
     // accumulated with atomicAdd), or nullptr.
     unsigned long long* trace;
@@ -243,9 +247,23 @@ struct KernelKey {
     int splitk;     // 1: fp32 partials per K slice into a workspace
 };
 
+// Row-class windows of a GEMM operand whose rows TMA cannot address (a row
+// pitch that is not a multiple of 16 bytes, or a misaligned base). Rows r
+// and r + 8 always lie a multiple of 16 bytes apart, so the rows of one
+// class q = r mod 8 form a tensor TMA can describe: its base is row q's
+// address rounded down to 16 bytes, its row stride 8 pitches, its width K
+// plus the class's offset (win_delta_*). A box 72 elements wide starting at
+// element 64 kb holds K block kb of every row of the class, shifted right by
+// that offset; the producer shifts it back in shared memory.
+struct WinMaps {
+    CUtensorMap a[8];
+    CUtensorMap b[8];
+};
+
 struct GemmLaunch {
     CUtensorMap mapA, mapB, mapC;
     CUtensorMap mapBh;  // B with narrow boxes (half or quarter height): the 2-SM, N = 256 narrow tail
+    WinMaps win;        // plain-load GEMM only
     GemmParams params;
     int grid;
     cudaStream_t stream;

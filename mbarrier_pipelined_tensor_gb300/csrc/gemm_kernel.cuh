@@ -22,17 +22,21 @@
 // t-1 overlap the mainloop of tile t (the "store k-1" of the steady state).
 //
 // Plain-load producer (LDG = true, 1-SM only): for operands TMA cannot
-// describe ("B200 Tma Pipeline Designer", step 1: keep the vectorized thread
-// copy), four producer warps (0 and 6-8) each own a quarter of a stage's
-// rows. A row's 64-element K segment starts at an address that is only
-// 2-byte aligned, so the warp copies the 144-byte window of 16-byte aligned
-// chunks around it with cp.async into a staging buffer (no registers hold
-// loads in flight; the copies of the next stage are issued before the
-// current one is unpacked), then shifts each row into place and writes it
-// in the same 128-byte-swizzled layout TMA would produce. Each warp fences
-// its generic-proxy writes for the tensor core's async-proxy reads and
-// makes one arrival on the stage's full barrier. The epilogue then writes C
-// with plain stores.
+// describe directly ("B200 Tma Pipeline Designer", step 1: keep the
+// vectorized thread copy). A row's 64-element K segment starts at an address
+// that is only 2-byte aligned, so the producer stages the 144-byte window of
+// 16-byte aligned chunks around it, then shifts each row into place and
+// writes it in the same 128-byte-swizzled layout TMA would produce; each
+// unpacking warp fences its generic-proxy writes for the tensor core's
+// async-proxy reads and makes one arrival on the stage's full barrier.
+//   GEMM: rows r and r + 8 of an operand lie a multiple of 16 bytes apart,
+//   so each row class r mod 8 is a tensor TMA can load (WinMaps). Warp 0's
+//   elected lane loads a stage's windows, 16 boxes of 72 x 16 elements, into
+//   one of three staging buffers; eight warps (6-13) unpack them.
+//   Conv: the im2col rows follow no such pattern; eight producer warps (0
+//   and 6-12) copy each row's window with cp.async (the copies of the next
+//   stage go out before the current one is unpacked), then unpack it. The
+//   epilogue writes the conv's C with plain stores.
 //
 // Atoms ("two-free-pipeline-stages" note): CG = 1 is the 1-SM atom (each CTA
 // owns a 128 x BN tile and holds all of its B tile); CG = 2 is the 2-SM atom
@@ -127,6 +131,34 @@ template <int B_ROWS>
 __host__ __device__ constexpr int ldg_staging_bytes()
 {
     return kLdgStaging * ldg_staging_buffer_bytes<B_ROWS>();
+}
+
+// The plain-load GEMM stages through row-class windows (WinMaps) instead:
+// a staging buffer holds a stage's rows as 144-byte windows that TMA writes
+// class by class (A: 8 classes of 16 rows, then B: 8 classes of B_ROWS / 8),
+// and the buffers' full / empty barriers follow them.
+constexpr int kWinRow = 144;
+constexpr int kWinStaging = 3;  // staging buffers: the window loads run two stages ahead
+constexpr int kWinStages = 2;   // ring stages (the tensor core drains one long before the next is unpacked)
+
+template <int B_ROWS>
+__host__ __device__ constexpr int win_staging_buffer_bytes()
+{
+    return (128 + B_ROWS) * kWinRow;
+}
+
+template <int B_ROWS>
+__host__ __device__ constexpr int win_staging_bytes()
+{
+    return kWinStaging * win_staging_buffer_bytes<B_ROWS>() + 64;
+}
+
+// Shared memory a plain-load variant adds to the ring: the conv gathers
+// with cp.async, the GEMM through row-class windows.
+template <int B_ROWS, bool CONV>
+__host__ __device__ constexpr int ldg_extra_bytes()
+{
+    return CONV ? ldg_staging_bytes<B_ROWS>() : win_staging_bytes<B_ROWS>();
 }
 
 // Row of the stage that lane `sub` (0..3) of a producer warp handles in row
@@ -301,6 +333,57 @@ __device__ __forceinline__ void ldg_repack_rows(uint32_t stg, int nvalid, uint32
     }
 }
 
+// Shifts the TMA-staged windows of stage rows [pw * RPW, pw * RPW + RPW)
+// into place (the plain-load GEMM). Operand row rr (class rr & 7, row
+// rr >> 3 of its class) is window (rr & 7) * rows / 8 + (rr >> 3) of the
+// operand's part of the buffer, its elements shifted right by the class's
+// offset; TMA has filled what lies past K or past the last row with zeros.
+// Lanes pair up as in ldg_repack_rows: the four rows of a quad are 8 apart,
+// so they share a class and a shift.
+template <int B_ROWS, int RPW>
+__device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint32_t dB, int pw, uint32_t lane,
+                                                uint32_t delta_a, uint32_t delta_b)
+{
+    const int sub = static_cast<int>(lane >> 3);
+    const uint32_t j = lane & 7u;
+    constexpr int kQuads = RPW / 4;
+    uint32_t mis[kQuads];
+    uint4 lo[kQuads], hi[kQuads];
+#pragma unroll
+    for (int q = 0; q < kQuads; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        const bool is_a = row < 128;
+        const int rr = is_a ? row : row - 128;
+        const int cls = rr & 7;
+        const int win = (is_a ? cls * 16 : 128 + cls * (B_ROWS / 8)) + (rr >> 3);
+        mis[q] = 2u * (((is_a ? delta_a : delta_b) >> (3 * cls)) & 7u);
+        const uint32_t src = stg + static_cast<uint32_t>(win) * kWinRow + 16u * j;
+        lo[q] = ld_shared_v4(src);
+        hi[q] = ld_shared_v4(src + 16u);
+    }
+#pragma unroll
+    for (int q = 0; q < kQuads; ++q) {
+        const int row = ldg_row(pw, RPW, q, sub);
+        uint32_t c[8] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w, hi[q].x, hi[q].y, hi[q].z, hi[q].w};
+        if (mis[q] & 8u) {
+#pragma unroll
+            for (int i = 0; i < 6; ++i) c[i] = c[i + 2];
+        }
+        if (mis[q] & 4u) {
+#pragma unroll
+            for (int i = 0; i < 5; ++i) c[i] = c[i + 1];
+        }
+        const uint32_t sh = (mis[q] & 2u) << 3;
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(c[k], c[k + 1], sh);
+        const int rr = row < 128 ? row : row - 128;
+        const uint32_t dst = (row < 128 ? dA : dB) + static_cast<uint32_t>(rr) * 128u +
+                             ((j ^ (static_cast<uint32_t>(rr) & 7u)) << 4);
+        st_shared_v4(dst, o[0], o[1], o[2], o[3]);
+    }
+}
+
 // Work unit u of a launch: output tile, its K-block range, and which part
 // of the tile's columns it covers (-1: the whole tile; else one of
 // p.tail_parts equal column parts of a narrow-tail tile).
@@ -352,21 +435,28 @@ __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, ui
     return ok;
 }
 
-// Threads of a mainloop CTA: producer, MMA issuer, four epilogue warps, and
-// with the plain-load producer three more producer warps.
-template <bool LDG>
+// Threads of a mainloop CTA: producer, MMA issuer, four epilogue warps;
+// with the plain-load producer kLdgWarps - 1 more producer warps (conv) or
+// kLdgWarps window-unpacking warps beside the window-loading warp 0 (GEMM).
+template <bool LDG, bool CONV = false>
 constexpr int mainloop_threads()
 {
-    return LDG ? 192 + 32 * (kLdgWarps - 1) : 192;
+    return !LDG ? 192 : (CONV ? 192 + 32 * (kLdgWarps - 1) : 192 + 32 * kLdgWarps);
 }
 
+struct NoWinMaps {
+    int unused;
+};
+
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
-__global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
+__global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapBh,
-                    const GemmParams p)
+                    const GemmParams p,
+                    const __grid_constant__ std::conditional_t<LDG && !CONV, WinMaps, NoWinMaps> wm)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
+    constexpr bool WIN = LDG && !CONV;  // the plain-load GEMM: row-class windows by TMA
     constexpr bool CL = (CG == 2);
     static_assert(!LDG || CG == 1, "the plain-load producer feeds the 1-SM atom");
     static_assert(!SPLITK || (OUT_F32 && !CONV && !LDG), "split-K writes fp32 GEMM partials");
@@ -405,6 +495,15 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
             mbar_init(acce_bar(b), Cfg::EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
+        if constexpr (WIN) {
+            // staging buffers: filled by the window loads (one expect_tx),
+            // freed by every unpacking warp
+            const uint32_t sw = sBar + Cfg::BAR_BYTES + kWinStaging * win_staging_buffer_bytes<Cfg::B_ROWS>();
+            for (int i = 0; i < kWinStaging; ++i) {
+                mbar_init(sw + 8u * i, 1);
+                mbar_init(sw + 8u * (kWinStaging + i), kLdgWarps);
+            }
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         if constexpr (!LDG) {
@@ -412,6 +511,13 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
             prefetch_tensormap(&mapB);
             prefetch_tensormap(&mapC);
             if (CG == 2 && BN == 256 && p.tail_units > 0) prefetch_tensormap(&mapBh);
+        }
+        if constexpr (WIN) {
+            for (int q = 0; q < 8; ++q) {
+                prefetch_tensormap(&wm.a[q]);
+                prefetch_tensormap(&wm.b[q]);
+            }
+            if (p.n_tma > 0) prefetch_tensormap(&mapC);
         }
     }
     if (warp == 1) {
@@ -435,9 +541,112 @@ __global__ void __launch_bounds__(mainloop_threads<LDG>(), 1)
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
-    if (LDG && (warp == 0 || warp >= 6)) {
+    if (WIN && warp == 0) {
+        // ------------------------- plain-load GEMM: window loads ---
+        if constexpr (WIN) {
+            if (elect_one()) {
+                constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS>());
+                constexpr int BPC = Cfg::B_ROWS / 8;  // B rows per class in a tile
+                const uint32_t sStg = sBar + Cfg::BAR_BYTES;
+                const uint32_t sw = sStg + kWinStaging * STG;
+                int slot = 0, issued = 0;
+                uint32_t sph = 0;
+                bool ok = true;
+                for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                    const Unit w = unit_of(u, num_tiles, p);
+                    int mt, nt;
+                    tile_coords(w.tile, p, mt, nt);
+                    // a tile's rows are whole classes' rows m0 / 8 .. m0 / 8 + 15
+                    const int ya = mt * (Cfg::BM / 8), yb = nt * BPC;
+                    for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                        const uint32_t fb = sw + 8u * slot;
+                        if (!wait_bounded(sw + 8u * (kWinStaging + slot), sph ^ 1u, p.wait, abort_flag,
+                                          SITE_PRODUCER_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(fb, STG);
+                        const uint32_t dst = sStg + slot * STG;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            tma_load_2d(dst + q * 16 * kWinRow, &wm.a[q], fb, kb * Cfg::BK, ya);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            tma_load_2d(dst + (128 + q * BPC) * kWinRow, &wm.b[q], fb, kb * Cfg::BK, yb);
+                        ++issued;
+                        if (++slot == kWinStaging) {
+                            slot = 0;
+                            sph ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) {
+                    // Gave up: let the loads in flight land first (bounded).
+                    volatile int no_abort = 0;
+                    const int n = issued < kWinStaging ? issued : kWinStaging;
+                    for (int i = 0; i < n; ++i) {
+                        if (--slot < 0) {
+                            slot = kWinStaging - 1;
+                            sph ^= 1u;
+                        }
+                        wait_bounded(sw + 8u * slot, sph, p.wait, &no_abort, SITE_DRAIN);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (WIN && warp >= 6) {
+        // ----------------------- plain-load GEMM: window unpacking ---
+        if constexpr (WIN) {
+            const int pw = warp - 6;
+            constexpr int RPW = (128 + Cfg::B_ROWS) / kLdgWarps;
+            constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS>());
+            const uint32_t sStg = sBar + Cfg::BAR_BYTES;
+            const uint32_t sw = sStg + kWinStaging * STG;
+            int s = 0, it = 0, slot = 0;
+            uint32_t ph = 0, sph = 0;
+            bool ok = true;
+            for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
+                const Unit w = unit_of(u, num_tiles, p);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    const uint32_t fb = sw + 8u * slot;
+                    int good = 1;
+                    if (lane == 0)
+                        good = wait_bounded(fb, sph, p.wait, abort_flag, SITE_COPY_FULL) &&
+                               wait_bounded(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
+                    if (!__shfl_sync(0xffffffffu, good, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    // lane 0 saw the windows land; the phase cannot move on
+                    // before this warp frees the buffer, so every lane's own
+                    // wait returns at once and orders its reads after the copy
+                    for (int i = 0; i < 1024 && !mbar_try_wait(fb, sph); ++i) {
+                    }
+                    win_repack_rows<Cfg::B_ROWS, RPW>(sStg + slot * STG, sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES,
+                                                      pw, lane, p.win_delta_a, p.win_delta_b);
+                    fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(full_bar(s));
+                        if (p.proto) proto_add(p.proto, static_cast<int>(blockIdx.x), PROTO_BAR_FULL, s, it / STAGES, 1);
+                        mbar_arrive(sw + 8u * (kWinStaging + slot));
+                    }
+                    ++it;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++slot == kWinStaging) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (LDG && (warp == 0 || warp >= 6)) {
         // ------------------------------------- plain-load producer ---
-        if constexpr (LDG) {
+        if constexpr (LDG && !WIN) {
             const int pw = warp == 0 ? 0 : warp - 5;  // producer warp 0..kLdgWarps-1 (warps 0, 6, 7, ...)
             constexpr int RPW = (128 + Cfg::B_ROWS) / kLdgWarps;
             constexpr uint32_t STG = static_cast<uint32_t>(ldg_staging_buffer_bytes<Cfg::B_ROWS>());
@@ -920,14 +1129,14 @@ template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false,
 cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
-    constexpr int SMEM = Cfg::SMEM_BYTES + (LDG ? ldg_staging_bytes<Cfg::B_ROWS>() : 0);
+    constexpr int SMEM = Cfg::SMEM_BYTES + (LDG ? ldg_extra_bytes<Cfg::B_ROWS, CONV>() : 0);
     auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>;
     static std::atomic<uint64_t> smem_set{0};
     cudaError_t e = smem_limit_once(kern, SMEM, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid), 1, 1);
-    cfg.blockDim = dim3(mainloop_threads<LDG>(), 1, 1);
+    cfg.blockDim = dim3(mainloop_threads<LDG, CONV>(), 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[2];
@@ -939,7 +1148,8 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params);
+    if constexpr (LDG && !CONV) return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, L.win);
+    else return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, NoWinMaps{0});
 }
 
 template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
@@ -948,7 +1158,7 @@ constexpr KernelEntry mainloop_entry()
     return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0, SPLITK ? 1 : 0},
                        &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>,
                        MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES +
-                           (LDG ? ldg_staging_bytes<MainloopCfg<CG, BN, STAGES, OUT_F32>::B_ROWS>() : 0)};
+                           (LDG ? ldg_extra_bytes<MainloopCfg<CG, BN, STAGES, OUT_F32>::B_ROWS, CONV>() : 0)};
 }
 
 }  // namespace tp

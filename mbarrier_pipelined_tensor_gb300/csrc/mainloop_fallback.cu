@@ -1,13 +1,13 @@
 // Plain-load producer variants of the mainloop (operands TMA cannot
-// describe): 1-SM atom, MMA N = 128, deepest ring, GEMM and conv, bf16 and
-// fp32 outputs.
+// describe): 1-SM atom, MMA N = 128, GEMM (row-class windows, 2 ring
+// stages) and conv (3), bf16 and fp32 outputs.
 #include "gemm_kernel.cuh"
 
 namespace tp {
 
 static const KernelEntry k_table[] = {
-    mainloop_entry<1, 128, 3, false, false, true>(),
-    mainloop_entry<1, 128, 3, true, false, true>(),
+    mainloop_entry<1, 128, 2, false, false, true>(),
+    mainloop_entry<1, 128, 2, true, false, true>(),
     mainloop_entry<1, 128, 3, false, true, true>(),
     mainloop_entry<1, 128, 3, true, true, true>(),
 };

@@ -280,6 +280,43 @@ def test_gemm_fallback_producer(M, N, K, lda, ldb, ldc, offs, out_f32):
     check_against_oracle(got[:, :N], ref, ab, out_f32, "fallback producer")
 
 
+@pytest.mark.parametrize("M,N,K,lda,ldb,offs", [
+    (5, 3, 100, 101, 103, (1, 1)),        # fewer than 8 rows: classes without rows
+    (8, 8, 64, 65, 66, (0, 0)),           # one row per class, one K block
+    (17, 300, 8, 9, 11, (0, 0)),          # K < 8: the window is mostly zero fill
+    (1000, 136, 200, 203, 207, (3, 7)),   # every class offset, ragged M and N tiles
+    (256, 384, 2000, 2001, 2005, (0, 2)),  # K tail 16 elements past a window boundary
+    (640, 520, 512, 512, 512, (1, 0)),    # aligned pitch, base 2 bytes off: one offset for all classes
+])
+def test_gemm_row_class_windows(M, N, K, lda, ldb, offs):
+    # The plain-load GEMM reads each row class (rows r mod 8) through its own
+    # TMA window; cover classes with no rows, every window offset, K and
+    # row tails, against the oracle and (fp32 C) bit for bit against the TMA
+    # producer on the same values.
+    A, B = datagen.gemm_operands(M, N, K, seed=M + K, lda=lda, ldb=ldb)
+    oa, ob = offs
+    a_all = dev_bf16(np.concatenate([np.zeros(oa, np.uint16), A.reshape(-1)]))
+    b_all = dev_bf16(np.concatenate([np.zeros(ob, np.uint16), B.reshape(-1)]))
+    c = new_out(M, N, True)
+    tp.tp_gemm_bf16_ex(a_all[oa:], b_all[ob:], c, M, N, K, lda, ldb, N, out_f32=True)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    ref, ab = oracle.gemm(A, B, M, N, K, lda, ldb)
+    got = host_f64(c)
+    check_against_oracle(got, ref, ab, True, "row-class windows")
+    if (K * 2) % 16 == 0:
+        # packed copies go through the TMA producer (one wave of tiles: it
+        # walks K forwards, as the plain loads do)
+        Ap = np.ascontiguousarray(A.reshape(M, lda)[:, :K])
+        Bp = np.ascontiguousarray(B.reshape(N, ldb)[:, :K])
+        c2 = new_out(M, N, True)
+        tp.tp_gemm_bf16_ex(dev_bf16(Ap), dev_bf16(Bp), c2, M, N, K, K, K, N, out_f32=True, atom=1, tile_n=128,
+                           pipe_depth=6)
+        expect_ok()
+        assert tp.tp_last_plan()["path"] == tp.TP_PATH_MAINLOOP
+        assert torch.equal(c, c2)
+
+
 @pytest.mark.parametrize("case", [(2, 9, 7, 3, 20, 3, 3, 1, 1), (1, 12, 11, 70, 66, 3, 3, 2, 1),
                                   (2, 6, 6, 12, 8, 1, 1, 1, 0)])
 def test_conv_fallback_producer(case):

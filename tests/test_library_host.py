@@ -100,9 +100,11 @@ def test_compiled_variants_match_budget():
     assert len(ks) >= 20
     for k in ks:
         st, b = tp.tp_query_smem_bytes(k["atom"], k["pipe_depth"], k["tile_n"], k["out_f32"])
-        # The plain-load producer adds two staging buffers: a stage's rows as
-        # 144-byte windows of aligned chunks plus a 4-byte code per row.
-        staging = 2 * (128 + k["tile_n"] // k["atom"]) * (144 + 4) if k["ldg"] else 0
+        # The plain-load producer adds staging buffers of a stage's rows
+        # as 144-byte windows: the conv's with a 4-byte code per row, the
+        # GEMM's (row-class windows by TMA) followed by their four barriers.
+        rows = 128 + k["tile_n"] // k["atom"]
+        staging = 0 if not k["ldg"] else (2 * rows * (144 + 4) if k["conv"] else 3 * rows * 144 + 64)
         assert st == tp.TP_OK and b + staging == k["smem_bytes"], k
         assert k["smem_bytes"] <= SMEM_LIMIT
     sweep = {(k["atom"], k["pipe_depth"]) for k in ks if k["tile_n"] == 128 and not k["conv"] and not k["out_f32"]}
@@ -198,7 +200,8 @@ def test_plan_tma_suitability():
     assert plan(64, 64, 64, C=AL + 2)[1]["path"] == ML                # C base: plain stores, TMA loads
     assert plan(64, 64, 64, B=AL + 2)[1]["path"] == FB
     st, p = plan(64, 64, 64, A=AL + 2)
-    assert st == tp.TP_OK and (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 128, 3)  # staging leaves 3 ring stages
+    # the GEMM's three window staging buffers leave 2 ring stages
+    assert st == tp.TP_OK and (p["atom"], p["tile_n"], p["pipe_depth"]) == (1, 128, 2)
     assert plan(64, 64, 64, A=AL + 1)[0] == tp.TP_ERR_INVALID_ARG     # a bf16 must be 2-byte aligned
     assert plan(64, 64, 64, C=AL + 2, out_f32=True)[0] == tp.TP_ERR_INVALID_ARG
     assert plan(64, 64, 64, A=AL + 2, atom=2)[0] == tp.TP_ERR_UNSUPPORTED
