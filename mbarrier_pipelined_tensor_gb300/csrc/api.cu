@@ -466,6 +466,24 @@ int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64
     return st;
 }
 
+// The kernels' FastDiv divisors, from the launch's tile counts and (conv)
+// extents; a divisor that does not apply is 1.
+void set_divisors(GemmParams& p)
+{
+    auto one = [](int64_t v) { return static_cast<uint32_t>(v > 0 ? v : 1); };
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int gm = std::max(1, p.group_m);
+    const int64_t groups = (p.m_tiles + gm - 1) / gm;
+    p.div_tiles = make_fastdiv(one(tiles));
+    p.div_group = make_fastdiv(one(static_cast<int64_t>(gm) * p.n_tiles));
+    p.div_gm = make_fastdiv(one(gm));
+    p.div_gm_last = make_fastdiv(one(p.m_tiles - (groups - 1) * gm));
+    p.div_pq = make_fastdiv(one(static_cast<int64_t>(p.conv_P) * p.conv_Q));
+    p.div_q = make_fastdiv(one(p.conv_Q));
+    p.div_cblocks = make_fastdiv(one(p.conv_cblocks));
+    p.div_s = make_fastdiv(one(p.conv_S));
+}
+
 int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
 {
     const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv,
@@ -474,6 +492,7 @@ int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
     if (!k) return TP_ERR_UNSUPPORTED;
     L.grid = pl.grid;
     L.stream = st;
+    set_divisors(L.params);
     cudaError_t e = k->launch(L);
     if (e != cudaSuccess) return cuda_fail(e);
     return TP_OK;
@@ -697,6 +716,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
         const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
         L.grid = pl.grid;
         L.stream = s;
+        set_divisors(p);
         cudaError_t e = k->launch(L);
         if (e != cudaSuccess) return cuda_fail(e);
         e = launch_splitk_reduce(static_cast<const float*>(ws), C, static_cast<int>(M), static_cast<int>(N), ldw,

@@ -87,6 +87,31 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     }
 }
 
+// Division by a divisor fixed for the launch, for 0 <= n < 2^31: with
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d) (which fits 32 bits),
+// n / d = (n * m) >> (31 + l) (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994, round-up method with
+// N = 31 bits). One wide multiply and a shift replace the division
+// sequence, which the kernels' single-thread roles would otherwise wait on
+// for every work unit.
+struct FastDiv {
+    uint32_t d, m;
+    uint32_t sh;
+};
+
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t top = 1ull << (31 + l);
+    return FastDiv{d, static_cast<uint32_t>((top + d - 1) / d), 31 + l};
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f)
+{
+    return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * f.m) >> f.sh);
+}
+
 // GEMM view of a launch. For the convolution M = N*P*Q output pixels,
 // N = output channels, K = R*S*C (walked as (r, s) outer, 64-channel blocks
 // inner).
@@ -112,6 +137,11 @@ struct GemmParams {
     // takes about a half or a quarter as long.
     int n_full, tail_units, tail_parts;
     int group_m;   // tile raster: group_m M-tiles share a sweep over N
+    // divisors of the unit and tile arithmetic (set_divisors): tiles
+    // (m_tiles * n_tiles), a raster group's tiles (group_m * n_tiles), its
+    // M-tiles (group_m, and the last group's), and the conv's P * Q, Q, 64-
+    // channel blocks and S
+    FastDiv div_tiles, div_group, div_gm, div_gm_last, div_pq, div_q, div_cblocks, div_s;
     int l2_a, l2_b;  // L2 eviction priority of A / B loads (0 normal, 1 first, 2 last)
     // convolution only
     int conv_P, conv_Q, conv_stride, conv_pad, conv_S, conv_cblocks;

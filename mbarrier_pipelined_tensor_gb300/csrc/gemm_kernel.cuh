@@ -89,15 +89,15 @@ struct MainloopCfg {
 
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mt, int& nt)
 {
-    const int group = p.group_m * p.n_tiles;
-    const int g = t / group;
+    const int g = fdiv(t, p.div_group);
     const int first = g * p.group_m;
-    const int gm = min(p.m_tiles - first, p.group_m);
-    const int r = t - g * group;
-    mt = first + r % gm;
+    // the last group may hold fewer M-tiles
+    const FastDiv& dgm = first + p.group_m > p.m_tiles ? p.div_gm_last : p.div_gm;
+    const int r = t - g * static_cast<int>(p.div_group.d);
     // odd groups sweep N from the far end, starting on the B columns the
     // group before ended on
-    const int n = r / gm;
+    const int n = fdiv(r, dgm);
+    mt = first + (r - n * static_cast<int>(dgm.d));
     nt = (g & 1) ? p.n_tiles - 1 - n : n;
 }
 
@@ -181,6 +181,7 @@ struct LdgRows {
     int64_t lda, ldb;
     int M, N, m_row, n_row, c0, r, sx, nvalid;
     int P, Q, H, W, C, R, S, stride, pad;
+    FastDiv div_pq, div_q;
 
     __device__ __forceinline__ LdgRows(const GemmParams& p, int m0, int n0, int kb)
         : A(p.A), B(p.B), lda(p.lda), ldb(p.ldb), M(p.M), N(p.N), m_row(m0), n_row(n0)
@@ -189,9 +190,9 @@ struct LdgRows {
         sx = 0;
         c0 = kb * 64;
         if constexpr (CONV) {
-            const int rs = kb / p.conv_cblocks;
+            const int rs = fdiv(kb, p.div_cblocks);
             c0 = (kb - rs * p.conv_cblocks) * 64;
-            r = rs / p.conv_S;
+            r = fdiv(rs, p.div_s);
             sx = rs - r * p.conv_S;
             P = p.conv_P;
             Q = p.conv_Q;
@@ -202,6 +203,8 @@ struct LdgRows {
             S = p.conv_S;
             stride = p.conv_stride;
             pad = p.conv_pad;
+            div_pq = p.div_pq;
+            div_q = p.div_q;
         }
         const int width = CONV ? p.conv_C : p.K;
         nvalid = (width - c0) < 64 ? (width - c0) : 64;  // >= 1: c0 < width
@@ -212,10 +215,9 @@ struct LdgRows {
         if (row < 128) {
             const int m = m_row + row;
             if constexpr (CONV) {
-                const int pq = P * Q;
-                const int img = m / pq;
-                const int rem = m - img * pq;
-                const int pp = rem / Q;
+                const int img = fdiv(m, div_pq);
+                const int rem = m - img * P * Q;
+                const int pp = fdiv(rem, div_q);
                 const int qq = rem - pp * Q;
                 const int h = pp * stride - pad + r;
                 const int w = qq * stride - pad + sx;
@@ -396,14 +398,14 @@ __device__ __forceinline__ Unit unit_of(int u, int num_tiles, const GemmParams& 
     Unit w;
     if (p.tail_units > 0 && u >= p.n_full) {
         const int v = u - p.n_full;
-        w.tile = p.n_full + v / p.tail_parts;
+        w.tile = p.n_full + (v >> (p.tail_parts == 4 ? 2 : 1));  // 2 or 4 parts
         w.part = v - (w.tile - p.n_full) * p.tail_parts;
         w.split = 0;
         w.kb0 = 0;
         w.kb1 = p.k_blocks;
         return w;
     }
-    w.split = u / num_tiles;
+    w.split = p.splits == 1 ? 0 : fdiv(u, p.div_tiles);
     w.tile = u - w.split * num_tiles;
     w.kb0 = w.split * p.kb_per_split;
     w.kb1 = min(p.k_blocks, w.kb0 + p.kb_per_split);
@@ -769,7 +771,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                     [[maybe_unused]] const int kb_flip = (plt & 1) ? w.kb0 + w.kb1 - 1 : -1;
                     [[maybe_unused]] int img = 0, base_h = 0, base_w = 0, rs = 0, cb = 0, r = 0, sx = 0;
                     if constexpr (CONV) {
-                        const int pq = p.conv_P * p.conv_Q;
+                        const int pq = static_cast<int>(p.div_pq.d);
                         img = m_row / pq;
                         const int rem = m_row - img * pq;
                         const int pp = rem / p.conv_Q;
@@ -1001,9 +1003,8 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
             const Unit w = unit_of(u, num_tiles, p);
             const int b = lt & 1;
             const uint32_t aph = static_cast<uint32_t>(lt >> 1) & 1u;
-            if (!timed_wait(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
-            if (p.events && warp == 2 && lane == 0) event_at(p, lt, EV_EPI_READY, globaltimer_ns());
-            tcgen05_fence_after();
+            // where the unit's outputs go: worked out before the wait, off
+            // the path from the last MMA to the stores
             int mt, nt;
             tile_coords(w.tile, p, mt, nt);
             const int m_row = mt * (Cfg::BM * CG) + static_cast<int>(rank) * Cfg::BM + quarter * 32;
@@ -1014,6 +1015,9 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                 nchunks = (p.N - n0 + Cfg::EPI_COLS - 1) / Cfg::EPI_COLS;
                 nchunks = nchunks < max_chunks ? nchunks : max_chunks;
             }
+            if (!timed_wait(p, accf_bar(b), aph, abort_flag, SITE_EPI_ACC_FULL, t_accf)) break;
+            if (p.events && warp == 2 && lane == 0) event_at(p, lt, EV_EPI_READY, globaltimer_ns());
+            tcgen05_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(b * BN);
             const uint32_t acce_target = CL ? mapa_shared(acce_bar(b), 0) : acce_bar(b);
@@ -1140,14 +1144,15 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // the 1-SM atom launches as plain CTAs, without a cluster shape
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CG;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = CG > 1 ? 2 : 1;
     if constexpr (LDG && !CONV) return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, L.win);
     else return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, NoWinMaps{0});
 }
