@@ -9,6 +9,8 @@ in seconds:
 * conv 32x56x56x256 * 3x3x256, stride 1, pad 1 (seed 2): every output of
   images 0 and 31 (all padding borders) plus 4096 random pixels.
 * 1 GiB copy (seed 4): bit-exact, compared on the device.
+* the plain-load producer at the benchmark's fallback row, 4096^3 with
+  lda = ldb = 4097 (seed 7): every 128th row plus the last.
 """
 import numpy as np
 import pytest
@@ -122,3 +124,19 @@ def test_copy_1gib_bit_exact():
     expect_ok()
     assert tp.tp_last_plan()["path"] == tp.TP_PATH_TMA_COPY
     assert torch.equal(src, dst)
+
+
+def test_plain_load_4096_odd_pitch_sampled():
+    # The benchmark's fallback row: odd pitches rule TMA out for A and B, so
+    # the 1-SM N = 128 mainloop is fed through the row-class windows.
+    M = N = K = 4096
+    ld = K + 1
+    A, B = datagen.gemm_operands(M, N, K, seed=7, dist="normal", lda=ld, ldb=ld)
+    rows = oracle.sample_rows(M, 128)
+    ref, ab = oracle.gemm(A, B, M, N, K, ld, ld, rows=rows)
+    c = new_out(M, N, False)
+    tp.tp_gemm_bf16_ex(dev_bf16(A), dev_bf16(B), c, M, N, K, ld, ld, N, atom=1, tile_n=128)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    got = host_f64(c.index_select(0, torch.from_numpy(rows).cuda()))
+    check_against_oracle(got, ref, ab, False, "plain-load 4096^3 odd pitches")
