@@ -395,7 +395,12 @@ TP_API int tp_tma_read_2d(const void* src, int64_t rows, int64_t cols, int64_t l
 TP_API int tp_device_status(void* stream);
 
 /* As tp_device_status, also reporting where the failure happened (site code,
- * block and thread); any output pointer may be NULL. */
+ * block and thread); any output pointer may be NULL. Sites: 1 a producer
+ * waiting for a free ring stage or staging buffer, 2 the MMA issuer waiting
+ * for a loaded stage, 3 the MMA issuer waiting for a drained accumulator,
+ * 4 the epilogue waiting for a finished accumulator, 5 a copy ring's or the
+ * plain-load GEMM's loads landing, 6 the wait for loads or MMAs in flight
+ * before a CTA exits, 7 the bounded-wait self test. */
 TP_API int tp_device_status_detail(void* stream, int* site, int* block, int* thread);
 
 /* Static string naming a tp_status value. */
