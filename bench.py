@@ -437,6 +437,13 @@ def measure_rows(torch, tp, stream, peaks, flush_buf):
         g()
     med, best = time_each_flushed(torch, stream, g, 50, flush_buf)
     rows["gemm_320x200x448_f32"] = {"unit": "us", "mean_us": round(med * 1e3, 2), "min_us": round(best * 1e3, 2)}
+    # The floor of the flushed timing itself: a one-element kernel timed the
+    # same way (events around the call, right after the L2 flush). Every
+    # flushed row carries about this much that is not the measured kernel.
+    tiny = torch.zeros(1, device="cuda")
+    med, best = time_each_flushed(torch, stream, lambda: tiny.add_(1), 50, flush_buf)
+    rows["flush_floor"] = {"unit": "us", "mean_us": round(med * 1e3, 2), "min_us": round(best * 1e3, 2),
+                           "what": "a one-element torch kernel timed like the flushed rows"}
 
     # The same small GEMMs back to back: eager launches from Python against a
     # CUDA graph of the same launches (no host cost per call; consecutive
@@ -710,6 +717,8 @@ def summarize(value, achieved, peak, rows, sweep, peaks):
         if sm:
             out["gemm_320x200x448_f32"] = {"us": sm["mean_us"],
                                            "cublas_us": lib.get("gemm_320x200x448", {}).get("us")}
+        if "flush_floor" in rows:
+            out["flush_floor_us"] = rows["flush_floor"]["mean_us"]
         for key, lk in (("tma_copy_1GiB", "copy_1GiB"), ("tma_transpose_1GiB", "transpose_1GiB")):
             r = rows.get(key)
             if r:
