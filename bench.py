@@ -517,6 +517,22 @@ def fallback_paths(torch, tp, stream, src, peaks):
                                  "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
                                  "bit_exact": bool(torch.equal(dst, src.t()))}
     del dst
+    # The tile transpose where it is needed: odd pitches on both sides (rows
+    # only 2-byte aligned), the same 32768 x 16384 elements.
+    lds, ldd = cc + 1, rr + 1
+    so = torch.empty((rr, lds), dtype=torch.int16, device="cuda")
+    so[:, :cc].copy_(src)
+    do = torch.empty((cc, ldd), dtype=torch.int16, device="cuda")
+    tro = lambda: tp.tp_tma_transpose_2d(so, do, rr, cc, lds, ldd, stream=s)  # noqa: E731
+    for _ in range(3):
+        tro()
+    ms = time_loop(torch, stream, tro, 20) / 20
+    out["vec_transpose_1GiB_odd_pitches"] = {
+        "unit": "GB/s", "gbs": round(moved / (ms * 1e-3) / 1e9, 1), "ld_src": lds, "ld_dst": ldd,
+        "tile_path": tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_TRANSPOSE,
+        "frac_of_hbm": round(moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+        "bit_exact": bool(torch.equal(do[:, :rr], src.t()))}
+    del so, do
     M = N = K = 4096
     flops = 2.0 * M * N * K
     gen = torch.Generator(device="cuda").manual_seed(7)
@@ -728,6 +744,9 @@ def summarize(value, achieved, peak, rows, sweep, peaks):
         if rs:
             out["tma_read_stream_256MiB"] = {"flushed_gbs": rs["flushed_gbs"], "b2b_gbs": rs["b2b_gbs"]}
         fb = rows.get("fallback_paths", {})
+        if "vec_transpose_1GiB" in fb:
+            out["tile_transpose_1GiB"] = {"gbs": fb["vec_transpose_1GiB"]["gbs"],
+                                          "odd_pitches_gbs": fb.get("vec_transpose_1GiB_odd_pitches", {}).get("gbs")}
         if "plain_load_producer_4096" in fb:
             out["plain_load_producer_4096"] = {"tflops": fb["plain_load_producer_4096"]["tflops"],
                                                "tma_tflops": fb["tma_producer_4096_same_variant"]["tflops"]}

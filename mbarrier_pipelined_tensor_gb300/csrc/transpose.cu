@@ -165,26 +165,109 @@ cudaError_t launch_tma_transpose(int stages, const CUtensorMap& s, const CUtenso
 // ------------------------------------------------------------ fallback ---
 
 // dst[c * ld_dst + r] = src[r * ld_src + c] for r in [r0, r0 + rows),
-// c < cols: 32x32 tiles through shared memory (one padding column against
-// bank conflicts), 32 x 8 threads.
+// c < cols, for operands TMA cannot describe: 64x64 tiles through shared
+// memory, 32 x 8 threads. A lane moves an element pair per row, as one
+// 4-byte access where the pair is 4-byte aligned and as two 2-byte accesses
+// otherwise. A thread's eight rows lie 8 pitches apart, a multiple of 16
+// bytes, so they share that alignment: the choice is made once per tile,
+// and all eight rows' loads are issued before any is used. Tile rows are
+// 65 elements apart, so the transposed reads (element k of rows 2 lx and
+// 2 lx + 1) hit distinct banks. Edge tiles check every element.
+constexpr int kVecT = 64;
+
 __global__ void __launch_bounds__(256)
     vec_transpose_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int64_t r0, int64_t rows,
                          int64_t cols, int64_t ld_src, int64_t ld_dst)
 {
-    __shared__ uint16_t tile[32][33];
-    const int64_t tiles_c = (cols + 31) / 32;
-    const int64_t tiles_r = (rows + 31) / 32;
+    __shared__ uint16_t tile[kVecT][kVecT + 1];
+    const int64_t tiles_c = (cols + kVecT - 1) / kVecT;
+    const int64_t tiles_r = (rows + kVecT - 1) / kVecT;
+    const int lx = static_cast<int>(threadIdx.x), ly = static_cast<int>(threadIdx.y);
+    const int64_t r_end = r0 + rows;
     for (int64_t t = blockIdx.x; t < tiles_c * tiles_r; t += gridDim.x) {
-        const int64_t tr = t / tiles_c, tc = t - (t / tiles_c) * tiles_c;
-        const int64_t rb = r0 + tr * 32, cb = tc * 32;
-        for (int k = threadIdx.y; k < 32; k += 8) {
-            const int64_t r = rb + k, c = cb + threadIdx.x;
-            if (r < r0 + rows && c < cols) tile[k][threadIdx.x] = src[r * ld_src + c];
+        const int64_t tr = t / tiles_c, tc = t - tr * tiles_c;
+        const int64_t rb = r0 + tr * kVecT, cb = tc * kVecT;
+        const bool full = rb + kVecT <= r_end && cb + kVecT <= cols;
+        // load: rows rb + ly + 8 i, columns cb + 2 lx, + 1
+        const uint16_t* p0 = src + (rb + ly) * ld_src + cb + 2 * lx;
+        if (full && (reinterpret_cast<uintptr_t>(p0) & 3u) == 0) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = __ldg(reinterpret_cast<const unsigned int*>(p0 + 8 * i * ld_src));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                tile[ly + 8 * i][2 * lx] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+                tile[ly + 8 * i][2 * lx + 1] = static_cast<uint16_t>(w[i] >> 16);
+            }
+        } else if (full) {
+            // The row starts 2 bytes past a 4-byte boundary: lane lx loads
+            // the aligned word holding elements 2 lx - 1 and 2 lx, and takes
+            // element 2 lx + 1 from the next lane's word (lane 31 from one
+            // more word). An aligned word holding one element of the row
+            // lies in that element's page, so the extra halves never fault.
+            const unsigned int* w0 = reinterpret_cast<const unsigned int*>(p0 - 1);
+            uint32_t w[8], e[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                w[i] = __ldg(w0 + 4 * i * ld_src);
+                e[i] = lx == 31 ? __ldg(w0 + 4 * i * ld_src + 1) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t nxt = __shfl_down_sync(0xffffffffu, w[i], 1);
+                if (lx == 31) nxt = e[i];
+                tile[ly + 8 * i][2 * lx] = static_cast<uint16_t>(w[i] >> 16);
+                tile[ly + 8 * i][2 * lx + 1] = static_cast<uint16_t>(nxt & 0xFFFFu);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t r = rb + ly + 8 * i, c = cb + 2 * lx;
+                uint16_t lo = 0, hi = 0;
+                if (r < r_end) {
+                    if (c < cols) lo = __ldg(p0 + 8 * i * ld_src);
+                    if (c + 1 < cols) hi = __ldg(p0 + 8 * i * ld_src + 1);
+                }
+                tile[ly + 8 * i][2 * lx] = lo;
+                tile[ly + 8 * i][2 * lx + 1] = hi;
+            }
         }
         __syncthreads();
-        for (int k = threadIdx.y; k < 32; k += 8) {
-            const int64_t c = cb + k, r = rb + threadIdx.x;
-            if (c < cols && r < r0 + rows) dst[c * ld_dst + r] = tile[threadIdx.x][k];
+        // store: dst rows cb + ly + 8 i, columns (source rows) rb + 2 lx, + 1
+        uint16_t* q0 = dst + (cb + ly) * ld_dst + rb + 2 * lx;
+        if (full && (reinterpret_cast<uintptr_t>(q0) & 3u) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = ly + 8 * i;
+                *reinterpret_cast<unsigned int*>(q0 + 8 * i * ld_dst) =
+                    static_cast<uint32_t>(tile[2 * lx][k]) | (static_cast<uint32_t>(tile[2 * lx + 1][k]) << 16);
+            }
+        } else if (full) {
+            // The row starts 2 bytes past a 4-byte boundary: lanes 1-31 each
+            // write the aligned word of elements 2 lx - 1 and 2 lx; the tile's
+            // first and last elements, whose words they share with the
+            // neighbouring tiles, are written alone.
+            unsigned int* qw = reinterpret_cast<unsigned int*>(q0 - 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = ly + 8 * i;
+                if (lx == 0)
+                    q0[8 * i * ld_dst] = tile[0][k];
+                else
+                    qw[4 * i * ld_dst] = static_cast<uint32_t>(tile[2 * lx - 1][k]) |
+                                         (static_cast<uint32_t>(tile[2 * lx][k]) << 16);
+                if (lx == 31) q0[8 * i * ld_dst + 1] = tile[kVecT - 1][k];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = ly + 8 * i;
+                const int64_t c = cb + k, r = rb + 2 * lx;
+                if (c < cols && r < r_end) {
+                    q0[8 * i * ld_dst] = tile[2 * lx][k];
+                    if (r + 1 < r_end) q0[8 * i * ld_dst + 1] = tile[2 * lx + 1][k];
+                }
+            }
         }
         __syncthreads();
     }
@@ -193,7 +276,7 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_vec_transpose(const void* src, void* dst, int64_t r0, int64_t rows, int64_t cols, int64_t ld_src,
                                  int64_t ld_dst, int sm_count, cudaStream_t st)
 {
-    const int64_t tiles = ((rows + 31) / 32) * ((cols + 31) / 32);
+    const int64_t tiles = ((rows + kVecT - 1) / kVecT) * ((cols + kVecT - 1) / kVecT);
     int64_t grid = static_cast<int64_t>(sm_count) * 8;
     if (grid > tiles) grid = tiles;
     if (grid < 1) grid = 1;

@@ -43,7 +43,9 @@ def test_tma_transpose_ring_shapes(stages, per_sm):
     assert plan["path"] == tp.TP_PATH_TMA_TRANSPOSE and plan["pipe_depth"] == stages
 
 
-@pytest.mark.parametrize("rows,cols,ld_src,ld_dst", [(100, 1001, 1001, 100), (33, 17, 19, 40), (500, 600, 600, 500)])
+@pytest.mark.parametrize("rows,cols,ld_src,ld_dst", [(100, 1001, 1001, 100), (33, 17, 19, 40), (500, 600, 600, 500),
+                                                     (129, 67, 70, 131), (64, 64, 65, 65), (1, 300, 300, 1),
+                                                     (300, 1, 1, 301)])
 def test_transpose_fallback(rows, cols, ld_src, ld_dst):
     plan = run_transpose(rows, cols, ld_src, ld_dst, seed=3)
     assert plan["path"] == tp.TP_PATH_VEC_TRANSPOSE or (rows * cols * 2 >= 65536 and plan["path"] ==
