@@ -218,7 +218,30 @@ cudaError_t launch_tma_read_any(int stages, const CUtensorMap& s, const CopyPara
 
 // ------------------------------------------------------------ fallback ---
 
+// Bytes sh .. sh + 15 of the 32 bytes lo:hi (sh even, 2..14): whole words
+// dropped with selects, then a 16-bit funnel shift.
+__device__ __forceinline__ uint4 shift_window16(const uint4& lo, const uint4& hi, uint32_t sh)
+{
+    uint32_t c[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    if (sh & 8u) {
+#pragma unroll
+        for (int i = 0; i < 6; ++i) c[i] = c[i + 2];
+    }
+    if (sh & 4u) {
+#pragma unroll
+        for (int i = 0; i < 5; ++i) c[i] = c[i + 1];
+    }
+    const uint32_t b = (sh & 2u) << 3;  // 0 or 16 bits
+    return make_uint4(__funnelshift_r(c[0], c[1], b), __funnelshift_r(c[1], c[2], b), __funnelshift_r(c[2], c[3], b),
+                      __funnelshift_r(c[3], c[4], b));
+}
+
 // rows x row_elems 2-byte elements, both buffers with pitch `pitch` elements.
+// Per row: 2-byte copies up to dst's first 16-byte boundary, then aligned
+// 16-byte stores. Where src has the same alignment the loads are aligned
+// 16-byte loads too; otherwise each store's 16 bytes are cut from the two
+// aligned source chunks around them (both hold bytes of the row, so neither
+// read can leave its page). The last partial chunk is copied by elements.
 __global__ void __launch_bounds__(256)
     vec_copy_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst, int64_t rows,
                     int64_t row_elems, int64_t pitch)
@@ -228,19 +251,21 @@ __global__ void __launch_bounds__(256)
         uint16_t* d = dst + r * pitch;
         const uintptr_t sa = reinterpret_cast<uintptr_t>(s);
         const uintptr_t da = reinterpret_cast<uintptr_t>(d);
-        int64_t head = row_elems;
-        int64_t nvec = 0;
-        if (((sa ^ da) & 15u) == 0) {
-            head = static_cast<int64_t>(((16u - (sa & 15u)) & 15u) / 2u);
-            if (head > row_elems) head = row_elems;
-            nvec = (row_elems - head) / 8;
-        }
+        int64_t head = static_cast<int64_t>(((16u - (da & 15u)) & 15u) / 2u);
+        if (head > row_elems) head = row_elems;
+        const int64_t nvec = (row_elems - head) / 8;
         const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
         const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
         for (int64_t i = tid; i < head; i += nthr) d[i] = s[i];
-        const uint4* sv = reinterpret_cast<const uint4*>(s + head);
         uint4* dv = reinterpret_cast<uint4*>(d + head);
-        for (int64_t i = tid; i < nvec; i += nthr) dv[i] = __ldg(sv + i);
+        const uintptr_t x = sa + 2u * static_cast<uintptr_t>(head);  // source of dst's first aligned chunk
+        const uint32_t sh = static_cast<uint32_t>(x & 15u);
+        const uint4* sv = reinterpret_cast<const uint4*>(x - sh);
+        if (sh == 0) {
+            for (int64_t i = tid; i < nvec; i += nthr) dv[i] = __ldg(sv + i);
+        } else {
+            for (int64_t i = tid; i < nvec; i += nthr) dv[i] = shift_window16(__ldg(sv + i), __ldg(sv + i + 1), sh);
+        }
         for (int64_t i = head + nvec * 8 + tid; i < row_elems; i += nthr) d[i] = s[i];
     }
 }

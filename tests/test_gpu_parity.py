@@ -76,6 +76,25 @@ def test_vectorized_fallback_copy(rows, cols, ld, offset):
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("rows,cols,ld,so,do", [(64, 600, 600, 1, 0), (50, 1001, 1003, 0, 3), (7, 9, 9, 2, 5),
+                                                 (33, 4096, 4097, 7, 1), (16, 100, 104, 4, 1), (5, 1, 3, 1, 6)])
+def test_vectorized_copy_relative_misalignment(rows, cols, ld, so, do):
+    # src and dst with different alignments: aligned 16-byte stores whose
+    # bytes are cut from two aligned source chunks.
+    total = rows * ld + 16
+    src_h = datagen.Stream(60 + so + do).bits16((total,))
+    src_all = dev_u16(src_h)
+    dst_all = torch.full_like(src_all, 0x1234)
+    tp.tp_tma_copy_2d(src_all[so:], dst_all[do:], rows, cols, ld)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_VEC_COPY
+    got = host_u16(dst_all)
+    want = np.full_like(src_h, 0x1234)
+    for r in range(rows):
+        want[do + r * ld:do + r * ld + cols] = src_h[so + r * ld:so + r * ld + cols]
+    assert np.array_equal(got, want)
+
+
 def test_forced_fallback_matches_tma():
     rows, cols = 512, 2048
     src_h = datagen.copy_source(rows, cols, seed=7)
