@@ -235,10 +235,11 @@ TP_API int tp_gemm_bf16_ex(const void* A, const void* B, void* C, int64_t M, int
  *              tp_gemm_splitk_workspace_bytes(M, N, splits) bytes; the call
  *              overwrites it. Calls that overlap on the GPU must not share a
  *              workspace. With one slice it is not touched (may be NULL).
- * A and B must be TMA-describable (16-byte aligned, lda*2 and ldb*2 multiples
- * of 16), else TP_ERR_UNSUPPORTED; C needs only natural alignment. A
- * workspace that is too small for an explicit `splits` returns
- * TP_ERR_INVALID_ARG. Two kernels are launched on `stream`.
+ * A and B that TMA cannot describe directly (misaligned bases, pitches not
+ * multiples of 8 elements) take the plain-load producer (1-SM atom, N = 128)
+ * with its row-class windows; C needs only natural alignment. A workspace
+ * that is too small for an explicit `splits` returns TP_ERR_INVALID_ARG. Two
+ * kernels are launched on `stream`.
  */
 TP_API int tp_gemm_bf16_splitk(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                                int64_t lda, int64_t ldb, int64_t ldc, int out_f32, int splits, void* workspace,

@@ -433,6 +433,17 @@ int encode_windows(CUtensorMap* maps, const void* X, int64_t K, int64_t rows, in
     return TP_OK;
 }
 
+// The split-K workspace as the epilogue's store map: `splits` slices of M
+// rows of ldw floats, 32 x 32 boxes.
+int encode_splitk_workspace(CUtensorMap* map, void* ws, int64_t ldw, int64_t M, int splits)
+{
+    TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws,
+                 {static_cast<uint64_t>(ldw), static_cast<uint64_t>(M), static_cast<uint64_t>(splits)},
+                 {static_cast<uint64_t>(ldw) * 4, static_cast<uint64_t>(M * ldw) * 4},
+                 {32, 32, 1}, CU_TENSOR_MAP_SWIZZLE_128B};
+    return encode_tiled(map, dw);
+}
+
 int gemm_plan_impl(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                    int64_t ldb, int64_t ldc, int out_f32, const tp_gemm_opts* opts, int sm_count, tp_plan* pl,
                    int splitk = 0)
@@ -610,8 +621,6 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     const int64_t ldw = splitk_ldw(N);
     int kps = static_cast<int>(pl.k_blocks);
     if (splitk) {
-        // Split-K feeds the mainloop through TMA only.
-        if (ldg) return TP_ERR_UNSUPPORTED;
         const int64_t slice_bytes = M * ldw * 4;
         const int64_t cap = (ws && slice_bytes > 0) ? ws_bytes / slice_bytes : 0;
         const int64_t tiles = pl.m_tiles * pl.n_tiles;
@@ -622,7 +631,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
         normalize_splits(pl.k_blocks, &sp, &kps);
         if (sp > 1) {
             if (sp > cap || (reinterpret_cast<uintptr_t>(ws) & 15u)) return TP_ERR_INVALID_ARG;
-            const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
+            const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, ldg ? 1 : 0, 1});
             if (!k) return TP_ERR_UNSUPPORTED;
             pl.splits = sp;
             int64_t units = tiles * sp;
@@ -651,7 +660,9 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
         if ((st = encode_windows(L.win.a, A, K, M, lda, 16, &p.win_delta_a)) ||
             (st = encode_windows(L.win.b, B, K, N, ldb, static_cast<uint32_t>(b_rows / 8), &p.win_delta_b)))
             return st;
-        if (c_tma) {
+        if (use_splitk) {
+            if ((st = encode_splitk_workspace(&L.mapC, ws, ldw, M, pl.splits))) return st;
+        } else if (c_tma) {
             TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
                          {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
                          {static_cast<uint64_t>(ldc) * eb}, {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
@@ -673,11 +684,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
             if ((st = encode_tiled(&L.mapBh, dbh))) return st;
         }
         if (use_splitk) {
-            TiledDesc dw{CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws,
-                         {static_cast<uint64_t>(ldw), static_cast<uint64_t>(M), static_cast<uint64_t>(pl.splits)},
-                         {static_cast<uint64_t>(ldw) * 4, static_cast<uint64_t>(M * ldw) * 4},
-                         {32, 32, 1}, CU_TENSOR_MAP_SWIZZLE_128B};
-            if ((st = encode_tiled(&L.mapC, dw))) return st;
+            if ((st = encode_splitk_workspace(&L.mapC, ws, ldw, M, pl.splits))) return st;
         } else if (c_tma) {
             TiledDesc dc{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C,
                          {static_cast<uint64_t>(n_tma > 0 ? n_tma : N), static_cast<uint64_t>(M)},
@@ -713,7 +720,7 @@ int gemm_impl(const void* A, const void* B, void* C, int64_t M, int64_t N, int64
     p.skip_commit = t_selftest_skip_commit;
     p.proto = opts ? opts->protocol : nullptr;
     if (use_splitk) {
-        const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, 0, 1});
+        const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, 1, 0, ldg ? 1 : 0, 1});
         L.grid = pl.grid;
         L.stream = s;
         set_divisors(p);

@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
     constexpr bool WIN = LDG && !CONV;  // the plain-load GEMM: row-class windows by TMA
     constexpr bool CL = (CG == 2);
     static_assert(!LDG || CG == 1, "the plain-load producer feeds the 1-SM atom");
-    static_assert(!SPLITK || (OUT_F32 && !CONV && !LDG), "split-K writes fp32 GEMM partials");
+    static_assert(!SPLITK || (OUT_F32 && !CONV), "split-K writes fp32 GEMM partials");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);

@@ -1,6 +1,6 @@
 // Plain-load producer variants of the mainloop (operands TMA cannot
 // describe): 1-SM atom, MMA N = 128, GEMM (row-class windows, 2 ring
-// stages) and conv (3), bf16 and fp32 outputs.
+// stages; also with split-K partials) and conv (3), bf16 and fp32 outputs.
 #include "gemm_kernel.cuh"
 
 namespace tp {
@@ -10,6 +10,7 @@ static const KernelEntry k_table[] = {
     mainloop_entry<1, 128, 2, true, false, true>(),
     mainloop_entry<1, 128, 3, false, true, true>(),
     mainloop_entry<1, 128, 3, true, true, true>(),
+    mainloop_entry<1, 128, 2, true, false, true, true>(),  // split-K partials
 };
 
 const KernelEntry* table_mainloop_fallback(int* n)

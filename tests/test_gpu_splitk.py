@@ -107,3 +107,21 @@ def test_splitk_errors():
     tp.tp_gemm_bf16_splitk(a, b, c, M, N, K, K, K, N, out_f32=True, splits=1, workspace=None)
     expect_ok()
     assert tp.tp_last_plan()["splits"] == 1
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_splitk_plain_load_producer(out_f32):
+    # Odd pitches: the K slices run on the plain-load producer's row-class
+    # windows and write their fp32 partials like the TMA producer's.
+    M, N, K, ld = 200, 384, 2500, 2503
+    A, B = datagen.gemm_operands(M, N, K, seed=71, lda=ld, ldb=ld)
+    a, b = dev_bf16(A), dev_bf16(B)
+    splits = 4
+    ws = torch.empty(tp.tp_gemm_splitk_workspace_bytes(M, N, splits) // 4, dtype=torch.float32, device="cuda")
+    c = new_out(M, N, out_f32)
+    tp.tp_gemm_bf16_splitk(a, b, c, M, N, K, ld, ld, N, out_f32=out_f32, splits=splits, workspace=ws)
+    expect_ok()
+    plan = tp.tp_last_plan()
+    assert plan["path"] == tp.TP_PATH_FALLBACK_MAINLOOP and plan["splits"] == splits
+    ref, ab = oracle.gemm(A, B, M, N, K, ld, ld)
+    check_against_oracle(host_f64(c), ref, ab, out_f32, "split-K plain-load")
