@@ -113,9 +113,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// The plain-load producer: producer warps, staging buffers (each holds a
+// The plain-load producer: producer (or, for the GEMM, unpacking) warps,
+// and for the conv's cp.async form its staging buffers (each holds a
 // stage's rows as 144-byte windows of aligned 16-byte chunks, then one
-// 32-bit code per row), and ring depth.
+// 32-bit code per row) and ring depth.
 constexpr int kLdgWarps = 8;
 constexpr int kLdgStaging = 2;
 constexpr int kLdgStages = 3;
