@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--pitch", type=int, default=0,
                     help="row pitch of A and B in elements for --only gemm (0 = K, the packed layout)")
     ap.add_argument("--conv-n", type=int, default=32, help="conv batch for --only conv")
+    ap.add_argument("--conv-c", type=int, default=256,
+                    help="input channels for --only conv (not a multiple of 8: the plain-load producer)")
     ap.add_argument("--copy-rows", type=int, default=32768, help="rows (x 16384) for --only copy/transpose")
     ap.add_argument("--gsweep", type=str, default="",
                     help="comma-separated group_m[:l2_hint] values: time a --steps loop of each")
@@ -830,14 +832,14 @@ def only_arm(args):
         work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s (flush included)"
         workload = f"gemm {M}x{N}x{K} lda=ldb={ld}"
     elif args.only == "conv":
-        N, H, W, C, K, R, S = args.conv_n, 56, 56, 256, 256, 3, 3
+        N, H, W, C, K, R, S = args.conv_n, 56, 56, args.conv_c, 256, 3, 3
         x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=2)
         xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
         wd = torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
         y = torch.empty((N * H * W, K), dtype=torch.bfloat16, device="cuda")
         fn = lambda: tp.tp_conv2d_fprop_bf16(xd, wd, y, N, H, W, C, K, R, S, 1, 1, stream=s)  # noqa: E731
         work, unit = 2.0 * N * H * W * K * R * S * C / 1e12, "TFLOP/s"
-        workload = f"conv {N}x56x56x256 * 3x3x256 stride 1 pad 1"
+        workload = f"conv {N}x56x56x{C} * 3x3x{C}, 256 filters, stride 1 pad 1"
     else:
         rr, cc = args.copy_rows, 16384
         src = torch.from_numpy(datagen.copy_source(rr, cc, seed=4).view(np.int16)).cuda()

@@ -317,7 +317,10 @@ TP_API int tp_gemm_bf16_host(const void* A_host, const void* B_host, void* C_hos
  * GEMM view: M = N*P*Q, N = K, K = R*S*C, walked as (r,s) outer, 64-channel
  * blocks inner. The im2col TMA producer needs C and K multiples of 8,
  * 16-byte aligned buffers, 1 <= stride <= 8, R, S <= 32 and pad < 128; other
- * problems take the plain-load producer.
+ * problems take the plain-load producer: for a stride-1 convolution whose
+ * output has the input's height and width, row-class TMA windows (pixels 8
+ * apart lie 16 C bytes apart) unpacked in shared memory; otherwise each
+ * row's window copied with cp.async.
  */
 TP_API int tp_conv2d_fprop_bf16(const void* x_nhwc, const void* w_krsc, void* y_nhwk, int64_t N, int64_t H, int64_t W,
                          int64_t C, int64_t K, int64_t R, int64_t S, int64_t stride, int64_t pad, void* stream);
@@ -453,7 +456,8 @@ TP_API int tp_last_plan(tp_plan* plan);
 /* One compiled mainloop variant. */
 typedef struct {
     int atom, pipe_depth, tile_n, out_f32, conv, smem_bytes;
-    int ldg;    /* 1: plain-load producer */
+    int ldg;    /* plain-load producer: 0 none (TMA), 1 GEMM row-class windows or conv cp.async
+                   windows, 2 conv row-class windows (stride 1, output the input's size) */
     int splitk; /* 1: split-K partials into a workspace */
 } tp_kernel_desc;
 

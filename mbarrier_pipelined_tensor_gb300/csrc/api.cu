@@ -164,6 +164,7 @@ int64_t mainloop_smem(int atom, int depth, int tile_n, int ldg = 0, int conv = 0
     const int64_t b = static_cast<int64_t>(tile_n / atom) * 64 * 2;
     const int64_t epi = 4 * 2 * 32 * 128;
     const int64_t staging = !ldg ? 0
+                            : ldg == kLdgConvWin ? static_cast<int64_t>(kWinStaging) * rows * kWinRowConv + 64
                             : conv ? static_cast<int64_t>(kLdgStaging) * rows * (kLdgWindow + 4)
                                    : static_cast<int64_t>(kWinStaging) * rows * kWinRow + 64;
     return 1024 + depth * (a + b) + epi + 256 + staging;
@@ -259,7 +260,8 @@ int plan_mainloop(int64_t M, int64_t N, int64_t k_blocks, int out_f32, int conv,
     // leaves room for kLdgStages ring stages (the GEMM's row-class windows:
     // kWinStages).
     int depth = o && o->pipe_depth ? o->pipe_depth
-                                   : (ldg ? (conv ? kLdgStages : kWinStages) : deepest_fitting(atom, tile_n));
+                                   : (ldg ? (conv && ldg == kLdgPlain ? kLdgStages : kWinStages)
+                                          : deepest_fitting(atom, tile_n));
     if (depth < 2 || depth > 9) return TP_ERR_INVALID_ARG;
     const int64_t smem = mainloop_smem(atom, depth, tile_n, ldg, conv);
     if (smem > kMaxSmemPerCta) return TP_ERR_SMEM_BUDGET;
@@ -415,7 +417,7 @@ void l2_hints_for(int mode, int* a, int* b)
 // zeros. A class with no rows (rows < 8) repeats class 0: the tile rows it
 // feeds lie past the last row and are never stored.
 int encode_windows(CUtensorMap* maps, const void* X, int64_t K, int64_t rows, int64_t ld, uint32_t box_rows,
-                   uint32_t* deltas)
+                   uint32_t* deltas, uint32_t box_cols = 72)
 {
     *deltas = 0;
     for (int q = 0; q < 8; ++q) {
@@ -425,7 +427,7 @@ int encode_windows(CUtensorMap* maps, const void* X, int64_t K, int64_t rows, in
         const uint32_t delta = static_cast<uint32_t>((row - base) / 2);
         TiledDesc d{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void*>(base),
                     {static_cast<uint64_t>(K + delta), static_cast<uint64_t>((rows - c + 7) / 8)},
-                    {static_cast<uint64_t>(ld) * 16}, {72, box_rows}, CU_TENSOR_MAP_SWIZZLE_NONE};
+                    {static_cast<uint64_t>(ld) * 16}, {box_cols, box_rows}, CU_TENSOR_MAP_SWIZZLE_NONE};
         const int st = encode_tiled(&maps[q], d);
         if (st) return st;
         *deltas |= delta << (3 * q);
@@ -495,10 +497,11 @@ void set_divisors(GemmParams& p)
     p.div_s = make_fastdiv(one(p.conv_S));
 }
 
-int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st)
+// ldg: the plain-load form of a fallback plan (kLdgPlain or kLdgConvWin).
+int launch_plan(const tp_plan& pl, GemmLaunch& L, cudaStream_t st, int ldg = kLdgPlain)
 {
     const KernelEntry* k = find_kernel(KernelKey{pl.atom, pl.tile_n, pl.pipe_depth, pl.out_f32, pl.conv,
-                                                 pl.path == TP_PATH_FALLBACK_MAINLOOP ? 1 : 0,
+                                                 pl.path == TP_PATH_FALLBACK_MAINLOOP ? ldg : 0,
                                                  pl.splits > 1 ? 1 : 0});
     if (!k) return TP_ERR_UNSUPPORTED;
     L.grid = pl.grid;
@@ -809,7 +812,12 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     // im2col TMA limits (cuTensorMapEncodeIm2col: rank-4 corners in
     // [-128, 127], traversal strides <= 8) and 16-byte byte strides;
     // otherwise the plain-load producer gathers the same tiles.
-    const int ldg = (C % 8 || !aligned16(x) || !aligned16(w) || stride > 8 || R > 32 || S > 32 || pad > 127) ? 1 : 0;
+    int ldg = (C % 8 || !aligned16(x) || !aligned16(w) || stride > 8 || R > 32 || S > 32 || pad > 127) ? kLdgPlain
+                                                                                                      : kLdgNone;
+    // A stride-1 convolution whose output is the input's size reads, for a
+    // tap, the pixels of a tile's outputs shifted by one offset: a run of
+    // consecutive pixels, which row-class windows can load.
+    if (ldg && stride == 1 && P == H && Q == W) ldg = kLdgConvWin;
     // y rows of whole 16-byte granules at a 16-byte aligned base go out by
     // TMA; otherwise the epilogue writes y with plain stores.
     const bool y_tma = aligned16(y) && (K * eb_out) % 16 == 0;
@@ -824,6 +832,21 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     GemmParams& p = L.params;
     // the narrow tail (2-SM, N = 256) before the maps: it sets their box
     if (!(opts && opts->no_tail)) set_narrow_tail(pl, p, opts, dev->sm_count);
+    if (ldg == kLdgConvWin) {
+        // rows: pixels (C elements each) and filters (R * S * C elements);
+        // 80-element boxes, since a filter's K blocks start anywhere
+        if ((st = encode_windows(L.win.a, x, C, N * H * W, C, 16, &p.win_delta_a, 80)) ||
+            (st = encode_windows(L.win.b, w, R * S * C, K, R * S * C, static_cast<uint32_t>(b_rows / 8),
+                                 &p.win_delta_b, 80)))
+            return st;
+        if (y_tma) {
+            const uint32_t eb = out_f32 ? 4 : 2;
+            TiledDesc dy{out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y,
+                         {static_cast<uint64_t>(K), static_cast<uint64_t>(M)}, {static_cast<uint64_t>(K) * eb},
+                         {128 / eb, 32}, CU_TENSOR_MAP_SWIZZLE_128B};
+            if ((st = encode_tiled(&L.mapC, dy))) return st;
+        }
+    }
     if (!ldg) {
         Im2colDesc dx{};
         dx.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -893,14 +916,15 @@ int tp_conv2d_fprop_bf16_ex(const void* x, const void* w, void* y, int64_t N, in
     p.conv_pad = static_cast<int>(pad);
     p.conv_S = static_cast<int>(S);
     p.conv_cblocks = static_cast<int>(cblocks);
-    p.n_tma = (ldg || !y_tma) ? 0 : static_cast<int>(K);  // TMA stores: rows are whole 16-byte granules
+    // TMA stores (rows of whole 16-byte granules) unless the cp.async form runs
+    p.n_tma = (ldg == kLdgPlain || !y_tma) ? 0 : static_cast<int>(K);
     p.trace = opts ? reinterpret_cast<unsigned long long*>(opts->trace) : nullptr;
     p.events = opts ? reinterpret_cast<unsigned long long*>(opts->events) : nullptr;
     p.proto = opts ? opts->protocol : nullptr;
     p.C = y;
     p.ldc_bytes = K * eb_out;
     p.wait = WaitCtl{dev->status, wait_limit_ns()};
-    st = launch_plan(pl, L, s);
+    st = launch_plan(pl, L, s, ldg ? ldg : kLdgPlain);
     if (st == TP_OK) t_last_plan = pl;
     return st;
 }

@@ -138,28 +138,35 @@ __host__ __device__ constexpr int ldg_staging_bytes()
 // a staging buffer holds a stage's rows as 144-byte windows that TMA writes
 // class by class (A: 8 classes of 16 rows, then B: 8 classes of B_ROWS / 8),
 // and the buffers' full / empty barriers follow them.
-constexpr int kWinRow = 144;
-constexpr int kWinStaging = 3;  // staging buffers: the window loads run two stages ahead
-constexpr int kWinStages = 2;   // ring stages (the tensor core drains one long before the next is unpacked)
+constexpr int kWinRow = 144;      // GEMM windows: 72 elements, K blocks start on 16-byte boundaries
+constexpr int kWinRowConv = 160;  // conv windows: 80 elements, a filter's K blocks need not
+constexpr int kWinStaging = 3;    // staging buffers: the window loads run two stages ahead
+constexpr int kWinStages = 2;     // ring stages (the tensor core drains one long before the next is unpacked)
 
-template <int B_ROWS>
+// Plain-load forms (the LDG template argument): 0 none (TMA producer), 1 the
+// GEMM's row-class windows or the conv's cp.async windows, 2 the conv's
+// row-class windows (stride 1, output the size of the input).
+constexpr int kLdgNone = 0, kLdgPlain = 1, kLdgConvWin = 2;
+
+template <int B_ROWS, int ROW>
 __host__ __device__ constexpr int win_staging_buffer_bytes()
 {
-    return (128 + B_ROWS) * kWinRow;
+    return (128 + B_ROWS) * ROW;
 }
 
-template <int B_ROWS>
+template <int B_ROWS, int ROW>
 __host__ __device__ constexpr int win_staging_bytes()
 {
-    return kWinStaging * win_staging_buffer_bytes<B_ROWS>() + 64;
+    return kWinStaging * win_staging_buffer_bytes<B_ROWS, ROW>() + 64;
 }
 
-// Shared memory a plain-load variant adds to the ring: the conv gathers
-// with cp.async, the GEMM through row-class windows.
-template <int B_ROWS, bool CONV>
+// Shared memory a plain-load variant adds to the ring: the conv's cp.async
+// staging, or the row-class windows of the GEMM or the conv.
+template <int B_ROWS, bool CONV, int LDG>
 __host__ __device__ constexpr int ldg_extra_bytes()
 {
-    return CONV ? ldg_staging_bytes<B_ROWS>() : win_staging_bytes<B_ROWS>();
+    return LDG == kLdgConvWin ? win_staging_bytes<B_ROWS, kWinRowConv>()
+                              : (CONV ? ldg_staging_bytes<B_ROWS>() : win_staging_bytes<B_ROWS, kWinRow>());
 }
 
 // Row of the stage that lane `sub` (0..3) of a producer warp handles in row
@@ -336,16 +343,33 @@ __device__ __forceinline__ void ldg_repack_rows(uint32_t stg, int nvalid, uint32
     }
 }
 
+// Per-stage facts the conv's row-class windows add: the tap's pixel offset
+// (input pixel of tile row t is pixel m0 + t + off), B's window start below
+// its K block (xd elements, 0..7), the valid channels of the K block, and
+// which of the lane's eight A rows lie inside the image (bit q).
+struct WinConvStage {
+    int off;
+    uint32_t xd;
+    int nvalid;
+    uint32_t row_ok;
+};
+
 // Shifts the TMA-staged windows of stage rows [pw * RPW, pw * RPW + RPW)
-// into place (the plain-load GEMM). Operand row rr (class rr & 7, row
-// rr >> 3 of its class) is window (rr & 7) * rows / 8 + (rr >> 3) of the
-// operand's part of the buffer, its elements shifted right by the class's
-// offset; TMA has filled what lies past K or past the last row with zeros.
-// Lanes pair up as in ldg_repack_rows: the four rows of a quad are 8 apart,
-// so they share a class and a shift.
-template <int B_ROWS, int RPW>
+// into place (row-class windows). B row rr (class rr & 7, row rr >> 3 of its
+// class) is window cls * rows / 8 + (rr >> 3) of B's part of the buffer. A
+// row t is window cls * 16 + (t >> 3) of A's part, cls = t & 7 for the GEMM
+// and (t + off) & 7 for the conv, whose pixels for a tap start `off` pixels
+// from the tile's. A window holds the row's elements shifted right by its
+// class's offset (plus, for the conv's B, xd), up to 30 bytes: output chunk
+// j is bytes mis .. mis + 15 of window chunks j + mis / 16 and the next.
+// TMA has zero-filled what lies past the end of a row or past the last
+// row; the conv also zeroes A rows outside the image (padding) and B
+// columns past the K block's channels (they belong to the next tap). Lanes
+// pair up as in ldg_repack_rows: the four rows of a quad are 8 apart, so
+// they share a class and a shift.
+template <int B_ROWS, int RPW, int ROW, bool CONVW>
 __device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint32_t dB, int pw, uint32_t lane,
-                                                uint32_t delta_a, uint32_t delta_b)
+                                                uint32_t delta_a, uint32_t delta_b, const WinConvStage& cs)
 {
     const int sub = static_cast<int>(lane >> 3);
     const uint32_t j = lane & 7u;
@@ -357,10 +381,13 @@ __device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint3
         const int row = ldg_row(pw, RPW, q, sub);
         const bool is_a = row < 128;
         const int rr = is_a ? row : row - 128;
-        const int cls = rr & 7;
+        const int cls = CONVW && is_a ? ((rr + cs.off) & 7) : (rr & 7);
         const int win = (is_a ? cls * 16 : 128 + cls * (B_ROWS / 8)) + (rr >> 3);
         mis[q] = 2u * (((is_a ? delta_a : delta_b) >> (3 * cls)) & 7u);
-        const uint32_t src = stg + static_cast<uint32_t>(win) * kWinRow + 16u * j;
+        if constexpr (CONVW) {
+            if (!is_a) mis[q] += 2u * cs.xd;
+        }
+        const uint32_t src = stg + static_cast<uint32_t>(win) * ROW + 16u * (j + (mis[q] >> 4));
         lo[q] = ld_shared_v4(src);
         hi[q] = ld_shared_v4(src + 16u);
     }
@@ -380,6 +407,18 @@ __device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint3
         uint32_t o[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(c[k], c[k + 1], sh);
+        if constexpr (CONVW) {
+            if (row < 128) {
+                if (!((cs.row_ok >> q) & 1u)) o[0] = o[1] = o[2] = o[3] = 0u;
+            } else if (cs.nvalid < 64) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int col = static_cast<int>(8u * j) + 2 * k;
+                    if (col >= cs.nvalid) o[k] = 0u;
+                    else if (col + 1 >= cs.nvalid) o[k] &= 0xFFFFu;
+                }
+            }
+        }
         const int rr = row < 128 ? row : row - 128;
         const uint32_t dst = (row < 128 ? dA : dB) + static_cast<uint32_t>(rr) * 128u +
                              ((j ^ (static_cast<uint32_t>(rr) & 7u)) << 4);
@@ -441,25 +480,35 @@ __device__ __forceinline__ bool timed_wait(const GemmParams& p, uint32_t bar, ui
 // Threads of a mainloop CTA: producer, MMA issuer, four epilogue warps;
 // with the plain-load producer kLdgWarps - 1 more producer warps (conv) or
 // kLdgWarps window-unpacking warps beside the window-loading warp 0 (GEMM).
-template <bool LDG, bool CONV = false>
-constexpr int mainloop_threads()
+template <int LDG, bool CONV = false>
+__host__ __device__ constexpr int mainloop_threads()
 {
-    return !LDG ? 192 : (CONV ? 192 + 32 * (kLdgWarps - 1) : 192 + 32 * kLdgWarps);
+    return !LDG ? 192 : ((CONV && LDG == kLdgPlain) ? 192 + 32 * (kLdgWarps - 1) : 192 + 32 * kLdgWarps);
 }
 
 struct NoWinMaps {
     int unused;
 };
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
+// Row-class windows are loaded by TMA: the plain-load GEMM, and the conv's
+// form for stride-1 convolutions whose output is the input's size.
+template <bool CONV, int LDG>
+__host__ __device__ constexpr bool win_form()
+{
+    return (LDG == kLdgPlain && !CONV) || LDG == kLdgConvWin;
+}
+
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, int LDG = kLdgNone, bool SPLITK = false>
 __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
     mainloop_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapBh,
                     const GemmParams p,
-                    const __grid_constant__ std::conditional_t<LDG && !CONV, WinMaps, NoWinMaps> wm)
+                    const __grid_constant__ std::conditional_t<win_form<CONV, LDG>(), WinMaps, NoWinMaps> wm)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
-    constexpr bool WIN = LDG && !CONV;  // the plain-load GEMM: row-class windows by TMA
+    constexpr bool WIN = win_form<CONV, LDG>();  // row-class windows by TMA
+    constexpr bool CWIN = LDG == kLdgConvWin;    // ... of a convolution
+    constexpr int WROW = CWIN ? kWinRowConv : kWinRow;
     constexpr bool CL = (CG == 2);
     static_assert(!LDG || CG == 1, "the plain-load producer feeds the 1-SM atom");
     static_assert(!SPLITK || (OUT_F32 && !CONV), "split-K writes fp32 GEMM partials");
@@ -501,7 +550,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
         if constexpr (WIN) {
             // staging buffers: filled by the window loads (one expect_tx),
             // freed by every unpacking warp
-            const uint32_t sw = sBar + Cfg::BAR_BYTES + kWinStaging * win_staging_buffer_bytes<Cfg::B_ROWS>();
+            const uint32_t sw = sBar + Cfg::BAR_BYTES + kWinStaging * win_staging_buffer_bytes<Cfg::B_ROWS, WROW>();
             for (int i = 0; i < kWinStaging; ++i) {
                 mbar_init(sw + 8u * i, 1);
                 mbar_init(sw + 8u * (kWinStaging + i), kLdgWarps);
@@ -545,10 +594,10 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
     if (WIN && warp == 0) {
-        // ------------------------- plain-load GEMM: window loads ---
+        // -------------------------------------- window loads ---
         if constexpr (WIN) {
             if (elect_one()) {
-                constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS>());
+                constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS, WROW>());
                 constexpr int BPC = Cfg::B_ROWS / 8;  // B rows per class in a tile
                 const uint32_t sStg = sBar + Cfg::BAR_BYTES;
                 const uint32_t sw = sStg + kWinStaging * STG;
@@ -560,7 +609,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                     int mt, nt;
                     tile_coords(w.tile, p, mt, nt);
                     // a tile's rows are whole classes' rows m0 / 8 .. m0 / 8 + 15
-                    const int ya = mt * (Cfg::BM / 8), yb = nt * BPC;
+                    const int m0 = mt * Cfg::BM, yb = nt * BPC;
                     for (int kb = w.kb0; kb < w.kb1; ++kb) {
                         const uint32_t fb = sw + 8u * slot;
                         if (!wait_bounded(sw + 8u * (kWinStaging + slot), sph ^ 1u, p.wait, abort_flag,
@@ -570,12 +619,29 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                         }
                         mbar_arrive_expect_tx(fb, STG);
                         const uint32_t dst = sStg + slot * STG;
+                        if constexpr (CWIN) {
+                            // K block kb is channels c0 .. c0 + 63 of tap (r, s). Tile
+                            // row t reads pixel m0 + t + off: for class q the rows
+                            // t = ((q - off) & 7) + 8 i, i < 16, a class-row run.
+                            const int rs = fdiv(kb, p.div_cblocks);
+                            const int c0 = (kb - rs * p.conv_cblocks) * Cfg::BK;
+                            const int r = fdiv(rs, p.div_s), sx = rs - r * p.conv_S;
+                            const int off = (r - p.conv_pad) * p.conv_W + (sx - p.conv_pad);
+                            const int xb = rs * p.conv_C + c0;  // the K block within a filter row
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            tma_load_2d(dst + q * 16 * kWinRow, &wm.a[q], fb, kb * Cfg::BK, ya);
+                            for (int q = 0; q < 8; ++q)
+                                tma_load_2d(dst + q * 16 * WROW, &wm.a[q], fb, c0, (m0 + off + ((q - off) & 7)) >> 3);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            tma_load_2d(dst + (128 + q * BPC) * kWinRow, &wm.b[q], fb, kb * Cfg::BK, yb);
+                            for (int q = 0; q < 8; ++q)
+                                tma_load_2d(dst + (128 + q * BPC) * WROW, &wm.b[q], fb, xb & ~7, yb);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                tma_load_2d(dst + q * 16 * WROW, &wm.a[q], fb, kb * Cfg::BK, m0 >> 3);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                tma_load_2d(dst + (128 + q * BPC) * WROW, &wm.b[q], fb, kb * Cfg::BK, yb);
+                        }
                         ++issued;
                         if (++slot == kWinStaging) {
                             slot = 0;
@@ -599,18 +665,35 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
             __syncwarp();
         }
     } else if (WIN && warp >= 6) {
-        // ----------------------- plain-load GEMM: window unpacking ---
+        // ------------------------------------ window unpacking ---
         if constexpr (WIN) {
             const int pw = warp - 6;
             constexpr int RPW = (128 + Cfg::B_ROWS) / kLdgWarps;
-            constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS>());
+            constexpr uint32_t STG = static_cast<uint32_t>(win_staging_buffer_bytes<Cfg::B_ROWS, WROW>());
             const uint32_t sStg = sBar + Cfg::BAR_BYTES;
             const uint32_t sw = sStg + kWinStaging * STG;
             int s = 0, it = 0, slot = 0;
             uint32_t ph = 0, sph = 0;
             bool ok = true;
+            WinConvStage cs{0, 0u, 64, 0xFFFFFFFFu};
             for (int u = cluster_id; ok && u < num_units; u += num_clusters) {
                 const Unit w = unit_of(u, num_tiles, p);
+                // conv, A warps: where the lane's eight rows (t = 32 pw + q + 8 sub)
+                // sit in the output image, minus the padding
+                [[maybe_unused]] int hq[8] = {}, wq[8] = {};
+                if (CWIN && pw < 4) {
+                    int mt, nt;
+                    tile_coords(w.tile, p, mt, nt);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int m = mt * Cfg::BM + pw * 32 + q + 8 * static_cast<int>(lane >> 3);
+                        const int img = fdiv(m, p.div_pq);
+                        const int rem = m - img * static_cast<int>(p.div_pq.d);
+                        const int pp = fdiv(rem, p.div_q);
+                        hq[q] = m < p.M ? pp - p.conv_pad : -(1 << 29);  // rows past M read as padding
+                        wq[q] = rem - pp * p.conv_Q - p.conv_pad;
+                    }
+                }
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     const uint32_t fb = sw + 8u * slot;
                     int good = 1;
@@ -626,8 +709,25 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                     // wait returns at once and orders its reads after the copy
                     for (int i = 0; i < 1024 && !mbar_try_wait(fb, sph); ++i) {
                     }
-                    win_repack_rows<Cfg::B_ROWS, RPW>(sStg + slot * STG, sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES,
-                                                      pw, lane, p.win_delta_a, p.win_delta_b);
+                    if constexpr (CWIN) {
+                        const int rs = fdiv(kb, p.div_cblocks);
+                        const int c0 = (kb - rs * p.conv_cblocks) * Cfg::BK;
+                        const int r = fdiv(rs, p.div_s), sx = rs - r * p.conv_S;
+                        cs.off = (r - p.conv_pad) * p.conv_W + (sx - p.conv_pad);
+                        cs.xd = static_cast<uint32_t>(rs * p.conv_C + c0) & 7u;
+                        cs.nvalid = p.conv_C - c0 < Cfg::BK ? p.conv_C - c0 : Cfg::BK;
+                        cs.row_ok = 0u;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int h = hq[q] + r, x = wq[q] + sx;
+                            if (static_cast<unsigned>(h) < static_cast<unsigned>(p.conv_H) &&
+                                static_cast<unsigned>(x) < static_cast<unsigned>(p.conv_W))
+                                cs.row_ok |= 1u << q;
+                        }
+                    }
+                    win_repack_rows<Cfg::B_ROWS, RPW, WROW, CWIN>(sStg + slot * STG, sA + s * Cfg::A_BYTES,
+                                                                  sB + s * Cfg::B_BYTES, pw, lane, p.win_delta_a,
+                                                                  p.win_delta_b, cs);
                     fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
                     __syncwarp();
                     if (lane == 0) {
@@ -647,7 +747,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                 }
             }
         }
-    } else if (LDG && (warp == 0 || warp >= 6)) {
+    } else if (LDG && !WIN && (warp == 0 || warp >= 6)) {
         // ------------------------------------- plain-load producer ---
         if constexpr (LDG && !WIN) {
             const int pw = warp == 0 ? 0 : warp - 5;  // producer warp 0..kLdgWarps-1 (warps 0, 6, 7, ...)
@@ -1130,11 +1230,11 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
     }
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, int LDG = kLdgNone, bool SPLITK = false>
 cudaError_t launch_mainloop(const GemmLaunch& L)
 {
     using Cfg = MainloopCfg<CG, BN, STAGES, OUT_F32>;
-    constexpr int SMEM = Cfg::SMEM_BYTES + (LDG ? ldg_extra_bytes<Cfg::B_ROWS, CONV>() : 0);
+    constexpr int SMEM = Cfg::SMEM_BYTES + (LDG ? ldg_extra_bytes<Cfg::B_ROWS, CONV, LDG>() : 0);
     auto kern = mainloop_kernel<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>;
     static std::atomic<uint64_t> smem_set{0};
     cudaError_t e = smem_limit_once(kern, SMEM, smem_set);
@@ -1154,17 +1254,18 @@ cudaError_t launch_mainloop(const GemmLaunch& L)
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CG > 1 ? 2 : 1;
-    if constexpr (LDG && !CONV) return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, L.win);
+    if constexpr (win_form<CONV, LDG>())
+        return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, L.win);
     else return cudaLaunchKernelEx(&cfg, kern, L.mapA, L.mapB, L.mapC, L.mapBh, L.params, NoWinMaps{0});
 }
 
-template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, bool LDG = false, bool SPLITK = false>
+template <int CG, int BN, int STAGES, bool OUT_F32, bool CONV, int LDG = kLdgNone, bool SPLITK = false>
 constexpr KernelEntry mainloop_entry()
 {
-    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG ? 1 : 0, SPLITK ? 1 : 0},
+    return KernelEntry{KernelKey{CG, BN, STAGES, OUT_F32 ? 1 : 0, CONV ? 1 : 0, LDG, SPLITK ? 1 : 0},
                        &launch_mainloop<CG, BN, STAGES, OUT_F32, CONV, LDG, SPLITK>,
                        MainloopCfg<CG, BN, STAGES, OUT_F32>::SMEM_BYTES +
-                           (LDG ? ldg_extra_bytes<MainloopCfg<CG, BN, STAGES, OUT_F32>::B_ROWS, CONV>() : 0)};
+                           (LDG ? ldg_extra_bytes<MainloopCfg<CG, BN, STAGES, OUT_F32>::B_ROWS, CONV, LDG>() : 0)};
 }
 
 }  // namespace tp

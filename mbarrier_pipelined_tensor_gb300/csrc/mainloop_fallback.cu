@@ -1,6 +1,7 @@
 // Plain-load producer variants of the mainloop (operands TMA cannot
 // describe): 1-SM atom, MMA N = 128, GEMM (row-class windows, 2 ring
-// stages; also with split-K partials) and conv (3), bf16 and fp32 outputs.
+// stages; also with split-K partials), conv (cp.async windows, 3; row-class
+// windows for stride-1 same-size convolutions, 2), bf16 and fp32 outputs.
 #include "gemm_kernel.cuh"
 
 namespace tp {
@@ -11,6 +12,8 @@ static const KernelEntry k_table[] = {
     mainloop_entry<1, 128, 3, false, true, true>(),
     mainloop_entry<1, 128, 3, true, true, true>(),
     mainloop_entry<1, 128, 2, true, false, true, true>(),  // split-K partials
+    mainloop_entry<1, 128, 2, false, true, kLdgConvWin>(),
+    mainloop_entry<1, 128, 2, true, true, kLdgConvWin>(),
 };
 
 const KernelEntry* table_mainloop_fallback(int* n)

@@ -403,6 +403,53 @@ def test_conv_output_channels_not_granular(out_f32):
     check_against_oracle(host_f64(y), ref, ab, out_f32, "conv K=100")
 
 
+CONV_WIN_CASES = [
+    # N, H, W, C, K, R, S, pad, (x offset, w offset) in elements
+    (2, 9, 7, 3, 20, 3, 3, 1, (0, 0)),
+    (1, 13, 11, 130, 136, 3, 3, 1, (0, 0)),   # three channel blocks, the last 2 wide
+    (2, 8, 8, 250, 256, 3, 3, 1, (1, 3)),     # odd channels, misaligned bases
+    (1, 10, 12, 64, 72, 5, 5, 2, (1, 0)),     # C a multiple of 8, x 2 bytes off
+    (3, 5, 5, 17, 9, 1, 1, 0, (0, 0)),        # 1x1
+    (1, 1, 3, 5, 4, 3, 3, 1, (0, 0)),         # fewer than 8 pixels and filters: empty classes
+    (4, 20, 18, 36, 140, 3, 3, 1, (2, 1)),    # 1440 pixels: several tiles, ragged last tile
+]
+
+
+@pytest.mark.parametrize("case", CONV_WIN_CASES)
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_conv_row_class_windows(case, out_f32):
+    # Stride-1 convolutions whose output is the input's size, on operands TMA
+    # cannot describe: the plain-load producer loads each tap's pixels and
+    # the filters through row-class windows, masking padding rows and the
+    # channels past C.
+    N, H, W, C, K, R, S, pad, (ox, ow) = case
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=N * H + C)
+    x_all = dev_bf16(np.concatenate([np.zeros(ox, np.uint16), x.reshape(-1)]))
+    w_all = dev_bf16(np.concatenate([np.zeros(ow, np.uint16), w.reshape(-1)]))
+    y = new_out(N * H * W, K, out_f32)
+    tp.tp_conv2d_fprop_bf16_ex(x_all[ox:], w_all[ow:], y, N, H, W, C, K, R, S, 1, pad, out_f32=out_f32)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, pad)
+    check_against_oracle(host_f64(y), ref, ab, out_f32, f"conv windows {case}")
+
+
+def test_conv_windows_match_tma_path_bit_for_bit():
+    # Only the base's alignment rules TMA out: both producers stage the same
+    # swizzled tiles in the same K order, so fp32 outputs agree exactly.
+    N, H, W, C, K, R, S = 2, 14, 13, 128, 256, 3, 3
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=88)
+    x_off = dev_bf16(np.concatenate([np.zeros(1, np.uint16), x.reshape(-1)]))[1:]
+    y1, y2 = new_out(N * H * W, K, True), new_out(N * H * W, K, True)
+    tp.tp_conv2d_fprop_bf16_ex(dev_bf16(x), dev_bf16(w), y1, N, H, W, C, K, R, S, 1, 1, out_f32=True, atom=1,
+                               tile_n=128)
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_MAINLOOP
+    tp.tp_conv2d_fprop_bf16_ex(x_off, dev_bf16(w), y2, N, H, W, C, K, R, S, 1, 1, out_f32=True)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    assert torch.equal(y1, y2)
+
+
 def test_fallback_matches_tma_path_bit_for_bit():
     # The same operands through both producers: the tensor core sees the same
     # swizzled stages, so the outputs are identical.

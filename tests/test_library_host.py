@@ -104,7 +104,12 @@ def test_compiled_variants_match_budget():
         # as 144-byte windows: the conv's with a 4-byte code per row, the
         # GEMM's (row-class windows by TMA) followed by their four barriers.
         rows = 128 + k["tile_n"] // k["atom"]
-        staging = 0 if not k["ldg"] else (2 * rows * (144 + 4) if k["conv"] else 3 * rows * 144 + 64)
+        if not k["ldg"]:
+            staging = 0
+        elif k["ldg"] == 2:        # the conv's row-class windows: 160-byte rows
+            staging = 3 * rows * 160 + 64
+        else:
+            staging = 2 * rows * (144 + 4) if k["conv"] else 3 * rows * 144 + 64
         assert st == tp.TP_OK and b + staging == k["smem_bytes"], k
         assert k["smem_bytes"] <= SMEM_LIMIT
     sweep = {(k["atom"], k["pipe_depth"]) for k in ks if k["tile_n"] == 128 and not k["conv"] and not k["out_f32"]}
