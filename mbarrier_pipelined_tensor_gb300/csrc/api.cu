@@ -164,7 +164,7 @@ int64_t mainloop_smem(int atom, int depth, int tile_n, int ldg = 0, int conv = 0
     const int64_t b = static_cast<int64_t>(tile_n / atom) * 64 * 2;
     const int64_t epi = 4 * 2 * 32 * 128;
     const int64_t staging = !ldg ? 0
-                            : ldg == kLdgConvWin ? static_cast<int64_t>(kWinStaging) * rows * kWinRowConv + 64
+                            : ldg == kLdgConvWin ? static_cast<int64_t>(kWinStaging) * (rows * kWinRowConv + 16) + 64
                             : conv ? static_cast<int64_t>(kLdgStaging) * rows * (kLdgWindow + 4)
                                    : static_cast<int64_t>(kWinStaging) * rows * kWinRow + 64;
     return 1024 + depth * (a + b) + epi + 256 + staging;

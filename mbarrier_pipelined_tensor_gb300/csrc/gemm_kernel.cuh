@@ -154,10 +154,12 @@ __host__ __device__ constexpr int win_staging_buffer_bytes()
     return (128 + B_ROWS) * ROW;
 }
 
+// The buffers, their full / empty barriers (64 bytes) and, for the conv,
+// one 16-byte record per buffer of its K block's tap facts (WinConvStage).
 template <int B_ROWS, int ROW>
 __host__ __device__ constexpr int win_staging_bytes()
 {
-    return kWinStaging * win_staging_buffer_bytes<B_ROWS, ROW>() + 64;
+    return kWinStaging * win_staging_buffer_bytes<B_ROWS, ROW>() + 64 + (ROW == kWinRowConv ? 16 * kWinStaging : 0);
 }
 
 // Shared memory a plain-load variant adds to the ring: the conv's cp.async
@@ -369,7 +371,7 @@ struct WinConvStage {
 // they share a class and a shift.
 template <int B_ROWS, int RPW, int ROW, bool CONVW>
 __device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint32_t dB, int pw, uint32_t lane,
-                                                uint32_t delta_a, uint32_t delta_b, const WinConvStage& cs)
+                                                uint32_t delta_a, uint32_t delta_b, const WinConvStage cs)
 {
     const int sub = static_cast<int>(lane >> 3);
     const uint32_t j = lane & 7u;
@@ -409,7 +411,9 @@ __device__ __forceinline__ void win_repack_rows(uint32_t stg, uint32_t dA, uint3
         for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(c[k], c[k + 1], sh);
         if constexpr (CONVW) {
             if (row < 128) {
-                if (!((cs.row_ok >> q) & 1u)) o[0] = o[1] = o[2] = o[3] = 0u;
+                const uint32_t keep = 0u - ((cs.row_ok >> q) & 1u);  // all ones or zero
+#pragma unroll
+                for (int k = 0; k < 4; ++k) o[k] &= keep;
             } else if (cs.nvalid < 64) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -617,7 +621,6 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(fb, STG);
                         const uint32_t dst = sStg + slot * STG;
                         if constexpr (CWIN) {
                             // K block kb is channels c0 .. c0 + 63 of tap (r, s). Tile
@@ -628,6 +631,13 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                             const int r = fdiv(rs, p.div_s), sx = rs - r * p.conv_S;
                             const int off = (r - p.conv_pad) * p.conv_W + (sx - p.conv_pad);
                             const int xb = rs * p.conv_C + c0;  // the K block within a filter row
+                            // the unpacking warps read these with the windows (the
+                            // arrival below releases them)
+                            const int nv = p.conv_C - c0 < Cfg::BK ? p.conv_C - c0 : Cfg::BK;
+                            st_shared_v4(sw + 64u + 16u * slot, static_cast<uint32_t>(off), static_cast<uint32_t>(xb & 7),
+                                         static_cast<uint32_t>(nv),
+                                         static_cast<uint32_t>(r) | (static_cast<uint32_t>(sx) << 16));
+                            mbar_arrive_expect_tx(fb, STG);
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 tma_load_2d(dst + q * 16 * WROW, &wm.a[q], fb, c0, (m0 + off + ((q - off) & 7)) >> 3);
@@ -635,6 +645,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                             for (int q = 0; q < 8; ++q)
                                 tma_load_2d(dst + (128 + q * BPC) * WROW, &wm.b[q], fb, xb & ~7, yb);
                         } else {
+                            mbar_arrive_expect_tx(fb, STG);
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 tma_load_2d(dst + q * 16 * WROW, &wm.a[q], fb, kb * Cfg::BK, m0 >> 3);
@@ -681,6 +692,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                 // conv, A warps: where the lane's eight rows (t = 32 pw + q + 8 sub)
                 // sit in the output image, minus the padding
                 [[maybe_unused]] int hq[8] = {}, wq[8] = {};
+                [[maybe_unused]] uint32_t tap_seen = 0xFFFFFFFFu;  // the tap row_ok was last worked out for
                 if (CWIN && pw < 4) {
                     int mt, nt;
                     tile_coords(w.tile, p, mt, nt);
@@ -710,19 +722,24 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                     for (int i = 0; i < 1024 && !mbar_try_wait(fb, sph); ++i) {
                     }
                     if constexpr (CWIN) {
-                        const int rs = fdiv(kb, p.div_cblocks);
-                        const int c0 = (kb - rs * p.conv_cblocks) * Cfg::BK;
-                        const int r = fdiv(rs, p.div_s), sx = rs - r * p.conv_S;
-                        cs.off = (r - p.conv_pad) * p.conv_W + (sx - p.conv_pad);
-                        cs.xd = static_cast<uint32_t>(rs * p.conv_C + c0) & 7u;
-                        cs.nvalid = p.conv_C - c0 < Cfg::BK ? p.conv_C - c0 : Cfg::BK;
-                        cs.row_ok = 0u;
+                        const uint4 rec = ld_shared_v4(sw + 64u + 16u * slot);
+                        const int r = static_cast<int>(rec.w & 0xFFFFu), sx = static_cast<int>(rec.w >> 16);
+                        cs.off = static_cast<int>(rec.x);
+                        cs.xd = rec.y;
+                        cs.nvalid = static_cast<int>(rec.z);
+                        if (rec.w != tap_seen) {
+                            // a new tap (the channel blocks of one tap share it)
+                            tap_seen = rec.w;
+                            uint32_t ok = 0u;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int h = hq[q] + r, x = wq[q] + sx;
-                            if (static_cast<unsigned>(h) < static_cast<unsigned>(p.conv_H) &&
-                                static_cast<unsigned>(x) < static_cast<unsigned>(p.conv_W))
-                                cs.row_ok |= 1u << q;
+                            for (int q = 0; q < 8; ++q) {
+                                const uint32_t in_h =
+                                    static_cast<uint32_t>(hq[q] + r) < static_cast<uint32_t>(p.conv_H);
+                                const uint32_t in_w =
+                                    static_cast<uint32_t>(wq[q] + sx) < static_cast<uint32_t>(p.conv_W);
+                                ok |= (in_h & in_w) << q;
+                            }
+                            cs.row_ok = ok;
                         }
                     }
                     win_repack_rows<Cfg::B_ROWS, RPW, WROW, CWIN>(sStg + slot * STG, sA + s * Cfg::A_BYTES,

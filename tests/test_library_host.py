@@ -106,8 +106,8 @@ def test_compiled_variants_match_budget():
         rows = 128 + k["tile_n"] // k["atom"]
         if not k["ldg"]:
             staging = 0
-        elif k["ldg"] == 2:        # the conv's row-class windows: 160-byte rows
-            staging = 3 * rows * 160 + 64
+        elif k["ldg"] == 2:        # the conv's row-class windows: 160-byte rows, a 16-byte record each
+            staging = 3 * (rows * 160 + 16) + 64
         else:
             staging = 2 * rows * (144 + 4) if k["conv"] else 3 * rows * 144 + 64
         assert st == tp.TP_OK and b + staging == k["smem_bytes"], k
