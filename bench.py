@@ -551,6 +551,21 @@ def fallback_paths(torch, tp, stream, src, peaks):
                      "path": "plain-load" if plan["path"] == tp.TP_PATH_FALLBACK_MAINLOOP else "tma",
                      "atom": plan["atom"], "tile_n": plan["tile_n"], "pipe_depth": plan["pipe_depth"]}
         del a, b, c
+    # The conv where channels are not a multiple of 8: the plain-load
+    # producer's row-class windows (stride 1, output the input's size).
+    Nc, H, W, K = 32, 56, 56, 256
+    for name, C in (("plain_load_conv_c250", 250), ("tma_conv_c256", 256)):
+        x = (torch.randn(Nc * H * W * C, device="cuda", generator=gen) * 0.02).bfloat16()
+        w = (torch.randn(K * 9 * C, device="cuda", generator=gen) * 0.02).bfloat16()
+        y = torch.empty((Nc * H * W, K), device="cuda", dtype=torch.bfloat16)
+        cv = lambda: tp.tp_conv2d_fprop_bf16(x, w, y, Nc, H, W, C, K, 3, 3, 1, 1, stream=s)  # noqa: E731
+        for _ in range(3):
+            cv()
+        ms = time_loop(torch, stream, cv, 10) / 10
+        plan = tp.tp_last_plan()
+        out[name] = {"unit": "TFLOP/s", "tflops": round(2.0 * Nc * H * W * K * 9 * C / (ms * 1e-3) / 1e12, 1),
+                     "C": C, "path": "plain-load" if plan["path"] == tp.TP_PATH_FALLBACK_MAINLOOP else "tma"}
+        del x, w, y
     return out
 
 
@@ -752,6 +767,9 @@ def summarize(value, achieved, peak, rows, sweep, peaks):
         if "plain_load_producer_4096" in fb:
             out["plain_load_producer_4096"] = {"tflops": fb["plain_load_producer_4096"]["tflops"],
                                                "tma_tflops": fb["tma_producer_4096_same_variant"]["tflops"]}
+        if "plain_load_conv_c250" in fb:
+            out["plain_load_conv_c250"] = {"tflops": fb["plain_load_conv_c250"]["tflops"],
+                                           "tma_c256_tflops": fb.get("tma_conv_c256", {}).get("tflops")}
     if sweep:
         sw = {}
         for r in sweep:

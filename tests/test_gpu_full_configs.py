@@ -10,7 +10,9 @@ in seconds:
   images 0 and 31 (all padding borders) plus 4096 random pixels.
 * 1 GiB copy (seed 4): bit-exact, compared on the device.
 * the plain-load producer at the benchmark's fallback row, 4096^3 with
-  lda = ldb = 4097 (seed 7): every 128th row plus the last.
+  lda = ldb = 4097 (seed 7): every 128th row plus the last; and the conv
+  fallback row, 32x56x56x250 * 3x3x250 (256 filters, seed 9): images 0 and
+  31 plus 2048 random pixels.
 """
 import numpy as np
 import pytest
@@ -140,3 +142,20 @@ def test_plain_load_4096_odd_pitch_sampled():
     assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
     got = host_f64(c.index_select(0, torch.from_numpy(rows).cuda()))
     check_against_oracle(got, ref, ab, False, "plain-load 4096^3 odd pitches")
+
+
+def test_plain_load_conv_c250_sampled():
+    # The benchmark's conv fallback row: 250 channels rule TMA out; the
+    # stride-1 same-size conv runs on row-class windows.
+    N, H, W, C, K, R, S = 32, 56, 56, 250, 256, 3, 3
+    x, w = datagen.conv_operands(N, H, W, C, K, R, S, seed=9)
+    pq = H * W
+    rng = np.random.default_rng(9)
+    pix = np.unique(np.concatenate([np.arange(pq), np.arange(31 * pq, 32 * pq), rng.integers(0, N * pq, 2048)]))
+    ref, ab = oracle.conv(x, w, N, H, W, C, K, R, S, 1, 1, pixels=pix)
+    y = new_out(N * pq, K, False)
+    tp.tp_conv2d_fprop_bf16(dev_bf16(x), dev_bf16(w), y, N, H, W, C, K, R, S, 1, 1)
+    expect_ok()
+    assert tp.tp_last_plan()["path"] == tp.TP_PATH_FALLBACK_MAINLOOP
+    got = host_f64(y.index_select(0, torch.from_numpy(pix).cuda()))
+    check_against_oracle(got, ref, ab, False, "conv 32x56x56x250 windows")
