@@ -412,6 +412,8 @@ CONV_WIN_CASES = [
     (3, 5, 5, 17, 9, 1, 1, 0, (0, 0)),        # 1x1
     (1, 1, 3, 5, 4, 3, 3, 1, (0, 0)),         # fewer than 8 pixels and filters: empty classes
     (4, 20, 18, 36, 140, 3, 3, 1, (2, 1)),    # 1440 pixels: several tiles, ragged last tile
+    (1, 30, 30, 19, 300, 3, 3, 1, (0, 5)),    # three filter tiles, the last ragged
+    (1, 16, 15, 40, 64, 7, 7, 3, (1, 1)),     # 7x7: 49 taps, offsets across three image rows
 ]
 
 
