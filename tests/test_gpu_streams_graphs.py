@@ -24,8 +24,10 @@ def _problem(seed):
     src = datagen.copy_source(300, 1000, seed=seed + 2)
     # odd pitches: the plain-load producer's row-class windows
     Ao, Bo = datagen.gemm_operands(M, N, K, seed=seed + 3, lda=K + 1, ldb=K + 1)
+    # 30 channels: the conv's row-class windows
+    xo, wo = datagen.conv_operands(2, 20, 18, 30, 64, 3, 3, seed=seed + 4)
     return dict(M=M, N=N, K=K, a=dev_bf16(A), b=dev_bf16(B), x=dev_bf16(x), w=dev_bf16(w), src=dev_u16(src),
-                ao=dev_bf16(Ao), bo=dev_bf16(Bo))
+                ao=dev_bf16(Ao), bo=dev_bf16(Bo), xo=dev_bf16(xo), wo=dev_bf16(wo))
 
 
 def _outputs(p):
@@ -34,6 +36,7 @@ def _outputs(p):
                 c3=torch.empty((p["M"], p["N"]), dtype=torch.bfloat16, device="cuda"),
                 c2=torch.empty((128, p["N"]), dtype=torch.bfloat16, device="cuda"),
                 y=torch.empty((2 * 20 * 18, 128), dtype=torch.bfloat16, device="cuda"),
+                yo=torch.empty((2 * 20 * 18, 64), dtype=torch.bfloat16, device="cuda"),
                 dst=torch.empty_like(p["src"]), t=torch.empty((1000, 300), dtype=torch.int16, device="cuda"), ws=ws)
 
 
@@ -44,12 +47,13 @@ def _enqueue(p, o, stream):
     tp.tp_gemm_bf16_splitk(p["a"], p["b"], o["c2"], 128, N, K, K, K, N, splits=4, workspace=o["ws"], stream=s)
     tp.tp_gemm_bf16_ex(p["ao"], p["bo"], o["c3"], M, N, K, K + 1, K + 1, N, stream=s)
     tp.tp_conv2d_fprop_bf16_ex(p["x"], p["w"], o["y"], 2, 20, 18, 64, 128, 3, 3, 1, 1, stream=s)
+    tp.tp_conv2d_fprop_bf16(p["xo"], p["wo"], o["yo"], 2, 20, 18, 30, 64, 3, 3, 1, 1, stream=s)
     tp.tp_tma_copy_2d(p["src"], o["dst"], 300, 1000, 1000, stream=s)
     tp.tp_tma_transpose_2d(p["src"], o["t"], 300, 1000, 1000, 300, stream=s)
 
 
 def _same(o1, o2):
-    for k in ("c", "c2", "c3", "y", "dst", "t"):
+    for k in ("c", "c2", "c3", "y", "yo", "dst", "t"):
         assert torch.equal(o1[k], o2[k]), k
 
 
