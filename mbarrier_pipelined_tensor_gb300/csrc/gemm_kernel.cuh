@@ -180,70 +180,55 @@ __device__ __forceinline__ int ldg_row(int pw, int rpw, int q, int sub)
     return pw * rpw + (q & 7) + 8 * (4 * (q >> 3) + sub);
 }
 
-// Where stage row `row` (A: rows 0..127, B: 128..) of K block kb comes
-// from: the address of its first element (0 when the row is out of range)
-// and the number of valid elements from there (1..64). The operand fields
-// are copied out of the kernel parameters once.
-template <bool CONV>
-struct LdgRows {
+// The conv's cp.async form: where stage row `row` (A: rows 0..127, the
+// im2col rows of output pixels; B: 128.., filters) of K block kb comes from:
+// the address of its first element (0 when the row is out of range or
+// padding) and the number of valid channels from there (1..64). The operand
+// fields are copied out of the kernel parameters once.
+struct ConvRows {
     const uint16_t* A;
     const uint16_t* B;
-    int64_t lda, ldb;
     int M, N, m_row, n_row, c0, r, sx, nvalid;
     int P, Q, H, W, C, R, S, stride, pad;
     FastDiv div_pq, div_q;
 
-    __device__ __forceinline__ LdgRows(const GemmParams& p, int m0, int n0, int kb)
-        : A(p.A), B(p.B), lda(p.lda), ldb(p.ldb), M(p.M), N(p.N), m_row(m0), n_row(n0)
+    __device__ __forceinline__ ConvRows(const GemmParams& p, int m0, int n0, int kb)
+        : A(p.A), B(p.B), M(p.M), N(p.N), m_row(m0), n_row(n0)
     {
-        r = 0;
-        sx = 0;
-        c0 = kb * 64;
-        if constexpr (CONV) {
-            const int rs = fdiv(kb, p.div_cblocks);
-            c0 = (kb - rs * p.conv_cblocks) * 64;
-            r = fdiv(rs, p.div_s);
-            sx = rs - r * p.conv_S;
-            P = p.conv_P;
-            Q = p.conv_Q;
-            H = p.conv_H;
-            W = p.conv_W;
-            C = p.conv_C;
-            R = p.conv_R;
-            S = p.conv_S;
-            stride = p.conv_stride;
-            pad = p.conv_pad;
-            div_pq = p.div_pq;
-            div_q = p.div_q;
-        }
-        const int width = CONV ? p.conv_C : p.K;
-        nvalid = (width - c0) < 64 ? (width - c0) : 64;  // >= 1: c0 < width
+        const int rs = fdiv(kb, p.div_cblocks);
+        c0 = (kb - rs * p.conv_cblocks) * 64;
+        r = fdiv(rs, p.div_s);
+        sx = rs - r * p.conv_S;
+        P = p.conv_P;
+        Q = p.conv_Q;
+        H = p.conv_H;
+        W = p.conv_W;
+        C = p.conv_C;
+        R = p.conv_R;
+        S = p.conv_S;
+        stride = p.conv_stride;
+        pad = p.conv_pad;
+        div_pq = p.div_pq;
+        div_q = p.div_q;
+        nvalid = (C - c0) < 64 ? (C - c0) : 64;  // >= 1: c0 < C
     }
 
     __device__ __forceinline__ uintptr_t segment(int row) const
     {
         if (row < 128) {
             const int m = m_row + row;
-            if constexpr (CONV) {
-                const int img = fdiv(m, div_pq);
-                const int rem = m - img * P * Q;
-                const int pp = fdiv(rem, div_q);
-                const int qq = rem - pp * Q;
-                const int h = pp * stride - pad + r;
-                const int w = qq * stride - pad + sx;
-                if (m >= M || h < 0 || h >= H || w < 0 || w >= W) return 0;
-                return reinterpret_cast<uintptr_t>(A + ((static_cast<int64_t>(img) * H + h) * W + w) * C + c0);
-            } else {
-                if (m >= M) return 0;
-                return reinterpret_cast<uintptr_t>(A + static_cast<int64_t>(m) * lda + c0);
-            }
+            const int img = fdiv(m, div_pq);
+            const int rem = m - img * P * Q;
+            const int pp = fdiv(rem, div_q);
+            const int qq = rem - pp * Q;
+            const int h = pp * stride - pad + r;
+            const int w = qq * stride - pad + sx;
+            if (m >= M || h < 0 || h >= H || w < 0 || w >= W) return 0;
+            return reinterpret_cast<uintptr_t>(A + ((static_cast<int64_t>(img) * H + h) * W + w) * C + c0);
         }
         const int n = n_row + (row - 128);
         if (n >= N) return 0;
-        if constexpr (CONV)
-            return reinterpret_cast<uintptr_t>(B + ((static_cast<int64_t>(n) * R + r) * S + sx) * C + c0);
-        else
-            return reinterpret_cast<uintptr_t>(B + static_cast<int64_t>(n) * ldb + c0);
+        return reinterpret_cast<uintptr_t>(B + ((static_cast<int64_t>(n) * R + r) * S + sx) * C + c0);
     }
 };
 
@@ -256,8 +241,8 @@ struct LdgRows {
 // (32 k + i) mod 9 of row (32 k + i) / 9. A chunk is copied only if it holds
 // at least one element of the row's valid range, so no access touches a
 // 16-byte block outside the operand (and none crosses a page).
-template <int B_ROWS, bool CONV, int RPW>
-__device__ __forceinline__ void ldg_issue_rows(const LdgRows<CONV>& rows, uint32_t stg, int pw, uint32_t lane)
+template <int B_ROWS, int RPW>
+__device__ __forceinline__ void ldg_issue_rows(const ConvRows& rows, uint32_t stg, int pw, uint32_t lane)
 {
     static_assert(RPW == 32, "one row per lane");
     const uint32_t codes = stg + (128 + B_ROWS) * kLdgWindow;
@@ -804,13 +789,13 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
             Use cur{0, 0, 0}, nxt{0, 0, 0};
             bool have_cur = fetch(cur);
             if (have_cur)
-                ldg_issue_rows<Cfg::B_ROWS, CONV, RPW>(LdgRows<CONV>(p, cur.m0, cur.n0, cur.kb), sStg, pw, lane);
+                ldg_issue_rows<Cfg::B_ROWS, RPW>(ConvRows(p, cur.m0, cur.n0, cur.kb), sStg, pw, lane);
             cp_async_commit();
             while (have_cur) {
                 // copies of the next use go out before this one is unpacked
                 const bool have_nxt = fetch(nxt);
                 if (have_nxt)
-                    ldg_issue_rows<Cfg::B_ROWS, CONV, RPW>(LdgRows<CONV>(p, nxt.m0, nxt.n0, nxt.kb),
+                    ldg_issue_rows<Cfg::B_ROWS, RPW>(ConvRows(p, nxt.m0, nxt.n0, nxt.kb),
                                                            sStg + (slot ^ 1u) * STG, pw, lane);
                 cp_async_commit();
                 cp_async_wait<1>();  // this use's copies (every lane's, after the warp sync)
@@ -819,7 +804,7 @@ __global__ void __launch_bounds__(mainloop_threads<LDG, CONV>(), 1)
                 if (lane == 0)
                     free_ok = wait_bounded(empty_bar(s), ph ^ 1u, p.wait, abort_flag, SITE_PRODUCER_EMPTY);
                 if (!__shfl_sync(0xffffffffu, free_ok, 0)) break;
-                ldg_repack_rows<Cfg::B_ROWS, RPW>(sStg + slot * STG, LdgRows<CONV>(p, cur.m0, cur.n0, cur.kb).nvalid,
+                ldg_repack_rows<Cfg::B_ROWS, RPW>(sStg + slot * STG, ConvRows(p, cur.m0, cur.n0, cur.kb).nvalid,
                                                   sA + s * Cfg::A_BYTES, sB + s * Cfg::B_BYTES, pw, lane);
                 fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
                 __syncwarp();
